@@ -1,0 +1,328 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks one oracle function against something independent: a
+hand-worked example, a library routine (numpy matmul, torch's bf16 conversion,
+torch autograd), a closed form, an invariant of the TwELL layout, brute force
+on tiny inputs, or central finite differences.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(vals):
+    out = []
+    for v in vals:
+        if v == "-0":
+            out.append(0x8000)
+        else:
+            out.append(int(torch.tensor([float(v)], dtype=torch.float32)
+                           .to(torch.bfloat16).view(torch.int16).item()) & 0xFFFF)
+    return np.array(out, dtype=np.uint16)
+
+
+def _torch_bf16_bits(a: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_f64(b):
+    return oracle.bf16_to_f64(b)
+
+
+# ------------------------------------------------------------------ rounding --
+
+def test_round_bf16_matches_torch():
+    rng = np.random.default_rng(1)
+    a = np.concatenate([
+        rng.standard_normal(100000).astype(np.float32),
+        (rng.standard_normal(10000) * 1e-38).astype(np.float32),       # subnormals
+        np.clip(rng.standard_normal(10000) * 1e38, -3.3e38, 3.3e38).astype(np.float32),  # near overflow
+        np.array([0.0, -0.0, np.inf, -np.inf, 1.0, 3.0e38], np.float32),
+    ])
+    # exact ties: low 16 bits == 0x8000 with odd and even kept parts
+    ties = (rng.integers(0, 2**15, 5000).astype(np.uint32) << 16) | 0x8000
+    a = np.concatenate([a, ties.view(np.float32)])
+    a = a[np.isfinite(a) | np.isinf(a)]
+    np.testing.assert_array_equal(oracle.round_bf16(a), _torch_bf16_bits(a))
+
+
+def test_round_bf16_nan_stays_nan():
+    out = oracle.round_bf16(np.array([np.nan, -np.nan], np.float32))
+    assert all((o & 0x7F80) == 0x7F80 and (o & 0x7F) != 0 for o in out)
+
+
+# ------------------------------------------------------------------- TwELL ---
+
+def test_pack_hand_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "twell_hand_example.json")))
+    h = np.stack([_bits(r) for r in g["h"]])
+    tw = oracle.twell_pack(h, g["T"])
+    np.testing.assert_array_equal(tw.nnz, g["nnz"])
+    np.testing.assert_array_equal(tw.K, g["K"])
+    np.testing.assert_array_equal(tw.off, g["off"])
+    np.testing.assert_array_equal(tw.idx, g["idx"])
+    np.testing.assert_array_equal(tw.val, np.array([int(v, 16) for v in g["val_bits"]], np.uint16))
+    W = np.stack([_bits(r) for r in g["W"]])
+    np.testing.assert_array_equal(oracle.twell_spmm(tw, W), np.array(g["y"], np.float64))
+
+
+def _brute_twell(h: np.ndarray, T: int):
+    """Independent brute force: python lists, built per tile from np.flatnonzero."""
+    M, F = h.shape
+    rows = [[int(j) for j in np.flatnonzero((h[r] & 0x7FFF) != 0)] for r in range(M)]
+    idx, val, K, off = [], [], [], [0]
+    for t0 in range(0, M, T):
+        band = rows[t0:t0 + T]
+        width = max((len(r) for r in band), default=0)
+        K.append(width)
+        for i, cols in enumerate(band):
+            padded = cols + [-1] * (width - len(cols))
+            idx += padded
+            val += [int(h[t0 + i, j]) if j >= 0 else 0 for j in padded]
+        off.append(len(idx))
+    return [len(r) for r in rows], K, off, idx, val
+
+
+@pytest.mark.parametrize("M,F,T,density,seed", [
+    (1, 1, 1, 1.0, 0), (7, 13, 3, 0.3, 1), (16, 40, 16, 0.1, 2), (33, 64, 8, 0.05, 3),
+    (20, 17, 100, 0.5, 4), (9, 31, 1, 0.2, 5), (12, 24, 5, 0.0, 6), (6, 10, 4, 1.0, 7)])
+def test_pack_matches_brute_force(M, F, T, density, seed):
+    h = syn.sparse_hidden(M, F, density, seed=seed)
+    tw = oracle.twell_pack(h, T)
+    nnz, K, off, idx, val = _brute_twell(h, T)
+    np.testing.assert_array_equal(tw.nnz, nnz)
+    np.testing.assert_array_equal(tw.K, K)
+    np.testing.assert_array_equal(tw.off, off)
+    np.testing.assert_array_equal(tw.idx, np.array(idx, np.int32))
+    np.testing.assert_array_equal(tw.val, np.array(val, np.uint16))
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 16, 64, 1000])
+def test_pack_invariants(T):
+    M, F = 150, 300
+    h = syn.sparse_hidden(M, F, 0.03, seed=11, row_skew_sigma=1.0)
+    # plant -0.0 entries: they must count as zero
+    h[::7, ::11] = np.where(h[::7, ::11] == 0, np.uint16(0x8000), h[::7, ::11])
+    tw = oracle.twell_pack(h, T)
+    code, back = oracle.twell_unpack(tw)
+    assert code == 0
+    np.testing.assert_array_equal(back, np.where(h == 0x8000, np.uint16(0), h))
+    n_tiles = (M + T - 1) // T
+    for t in range(n_tiles):
+        band = tw.nnz[t * T:(t + 1) * T]
+        assert tw.K[t] == band.max()
+        assert tw.off[t + 1] - tw.off[t] == len(band) * tw.K[t]
+    assert tw.off[0] == 0 and tw.slots == sum(
+        min(T, M - t * T) * tw.K[t] for t in range(n_tiles))
+    np.testing.assert_array_equal(tw.nnz, ((h & 0x7FFF) != 0).sum(1))
+
+
+def test_pack_special_cases():
+    M, F = 20, 30
+    h = syn.sparse_hidden(M, F, 0.2, seed=5)
+    # T = 1: exact per-row ELL (no padding at all)
+    tw1 = oracle.twell_pack(h, 1)
+    np.testing.assert_array_equal(tw1.K, tw1.nnz)
+    assert (tw1.idx >= 0).all()
+    # T >= M: classic ELL, one global width
+    twM = oracle.twell_pack(h, M + 5)
+    assert twM.K.tolist() == [tw1.nnz.max()] and twM.slots == M * tw1.nnz.max()
+    # all active: K = F and the values are a row-major copy
+    full = syn.sparse_hidden(M, F, 1.0, seed=6)
+    twf = oracle.twell_pack(full, 4)
+    assert (twf.K == F).all()
+    np.testing.assert_array_equal(twf.val, full.reshape(-1))
+    np.testing.assert_array_equal(twf.idx, np.tile(np.arange(F), M))
+    # nothing active
+    tw0 = oracle.twell_pack(np.zeros((M, F), np.uint16), 4)
+    assert tw0.slots == 0 and (tw0.K == 0).all()
+
+
+def test_unpack_rejects_malformed():
+    h = syn.sparse_hidden(10, 20, 0.3, seed=9)
+    tw = oracle.twell_pack(h, 4)
+    bad = oracle.Twell(**{**tw.__dict__, "idx": tw.idx.copy()})
+    row_start = 0
+    assert tw.nnz[0] >= 2
+    bad.idx[row_start], bad.idx[row_start + 1] = bad.idx[row_start + 1], bad.idx[row_start]
+    assert oracle.twell_unpack(bad)[0] == 6
+    bad2 = oracle.Twell(**{**tw.__dict__, "K": tw.K + 1})
+    assert oracle.twell_unpack(bad2)[0] in (2, 3)
+
+
+# ------------------------------------------------------------ forward path ---
+
+def test_preactivation_matches_numpy_matmul():
+    inp = syn.ffn_inputs(24, 96, 200, 8, -0.5, seed=3)
+    out = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, 24, 96, 200)
+    ref = (_bf16_f64(inp.x) @ _bf16_f64(inp.W_up).T).astype(np.float32) + inp.b
+    # fp64 sums in two different orders round to the same fp32 except at ties
+    ulp = np.spacing(np.abs(ref).astype(np.float32))
+    assert np.all(np.abs(out["pre"] - ref) <= ulp)
+    np.testing.assert_array_equal(out["h"], _torch_bf16_bits(np.where(out["pre"] > 0, out["pre"], 0)))
+    y_ref = _bf16_f64(out["h"]) @ _bf16_f64(inp.W_down)
+    np.testing.assert_allclose(out["y"], y_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_integer_inputs_are_exact():
+    inp = syn.integer_ffn_inputs(40, 64, 96, 16, seed=2, bias=-6)
+    out = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, 40, 64, 96)
+    xi = _bf16_f64(inp.x).astype(np.int64)
+    wi = _bf16_f64(inp.W_up).astype(np.int64)
+    pre = (xi @ wi.T - 6).astype(np.float32)
+    np.testing.assert_array_equal(out["pre"], pre)
+    h_ref = _torch_bf16_bits(np.maximum(pre, 0))
+    np.testing.assert_array_equal(out["h"], h_ref)
+    np.testing.assert_array_equal(out["active"], (h_ref != 0).astype(np.uint8))
+
+
+def test_gated_forward_matches_torch():
+    inp = syn.ffn_inputs(16, 64, 128, 16, -0.3, seed=4, gated=True)
+    out = oracle.ffn_fwd_rows(inp.x, inp.W_up, inp.W_gate, inp.b, inp.W_down, 16, 64, 128)
+    x = torch.from_numpy(_bf16_f64(inp.x))
+    g = (x @ torch.from_numpy(_bf16_f64(inp.W_gate)).T).float() + torch.from_numpy(inp.b)
+    u = (x @ torch.from_numpy(_bf16_f64(inp.W_up)).T).float()
+    ulp_g = torch.from_numpy(np.spacing(np.abs(g.numpy())))
+    assert torch.all((torch.from_numpy(out["pre"]) - g).abs() <= ulp_g)
+    np.testing.assert_array_equal(out["active"], (out["pre"] > 0).astype(np.uint8))
+    pre, uo = torch.from_numpy(out["pre"]), torch.from_numpy(out["u"])
+    ulp_u = torch.from_numpy(np.spacing(np.abs(u.numpy())))
+    assert torch.all((uo - u).abs() <= ulp_u)
+    h_ref = torch.where(pre > 0, pre * uo, torch.zeros(())).to(torch.bfloat16)
+    np.testing.assert_array_equal(out["h"], h_ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_gated_pack_uses_gate_support():
+    inp = syn.ffn_inputs(8, 32, 64, 4, -0.2, seed=8, gated=True)
+    out = oracle.ffn_fwd_rows(inp.x, inp.W_up, inp.W_gate, inp.b, inp.W_down, 8, 32, 64)
+    h = out["h"].copy()
+    act = out["active"]
+    j = np.argwhere(act)[0]
+    h[tuple(j)] = 0  # a stored slot whose value is +0 (u == 0 case)
+    tw = oracle.twell_pack(h, 4, active=act)
+    np.testing.assert_array_equal(tw.nnz, act.sum(1))
+    code, back = oracle.twell_unpack(tw)
+    assert code == 0
+    np.testing.assert_array_equal(back, h)
+
+
+@pytest.mark.parametrize("M,F,T,d,density", [(30, 50, 4, 16, 0.1), (64, 512, 16, 128, 0.01),
+                                             (5, 9, 1, 3, 0.6), (17, 40, 32, 24, 0.0)])
+def test_sparse_product_equals_dense_product(M, F, T, d, density):
+    h = syn.sparse_hidden(M, F, density, seed=M + F)
+    W = syn.to_bf16_bits(syn.normal(3, 9, F * d).reshape(F, d).astype(np.float32))
+    tw = oracle.twell_pack(h, T)
+    y = oracle.twell_spmm(tw, W)
+    np.testing.assert_allclose(y, _bf16_f64(h) @ _bf16_f64(W), rtol=1e-12, atol=1e-12)
+
+
+def test_hidden_density_matches_closed_form():
+    # pre = x.w + b with x ~ N(0,1)^d, w ~ N(0,1/d)^d is close to N(b, 1), so the
+    # active fraction is close to 1 - Phi(-b) = Phi(b).
+    M, d, F = 96, 512, 2048
+    for bias in (-2.33, -1.2816):
+        inp = syn.ffn_inputs(M, d, F, 16, bias, seed=0)
+        out = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F,
+                                  want_y=False)
+        dens = out["active"].mean()
+        expect = 0.5 * math.erfc(-bias / math.sqrt(2.0))
+        assert abs(dens - expect) < 0.15 * expect, (bias, dens, expect)
+
+
+# --------------------------------------------------------------- backward ----
+
+def _fd_setup(seed=0, M=4, d=6, F=10, l1=0.05):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, d))
+    Wu = rng.standard_normal((F, d)) / math.sqrt(d)
+    Wd = rng.standard_normal((F, d)) / math.sqrt(F)
+    b = rng.standard_normal(F) * 0.5
+    dy = rng.standard_normal((M, d))
+    pre = x @ Wu.T + b
+    assert np.abs(pre).min() > 1e-3  # stay away from the ReLU kink
+    return x, Wu, b, Wd, dy, l1
+
+
+def test_backward_matches_finite_differences():
+    x, Wu, b, Wd, dy, l1 = _fd_setup()
+    L, h = oracle.ffn_loss_f64(x, Wu, b, Wd, dy, l1, want_h=True)
+    dpre, dx = oracle.ffn_bwd_rows(x, Wu, Wd, h, dy, l1)
+    gu, gd, gb = oracle.ffn_bwd_cols(x, Wu, Wd, h, dy, l1)
+    eps = 1e-6
+
+    def fd(arr, setter):
+        g = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            a = arr.copy(); a[i] += eps; Lp = setter(a)
+            a = arr.copy(); a[i] -= eps; Lm = setter(a)
+            g[i] = (Lp - Lm) / (2 * eps)
+        return g
+
+    np.testing.assert_allclose(fd(x, lambda a: oracle.ffn_loss_f64(a, Wu, b, Wd, dy, l1)), dx, atol=1e-7)
+    np.testing.assert_allclose(fd(Wu, lambda a: oracle.ffn_loss_f64(x, a, b, Wd, dy, l1)), gu, atol=1e-7)
+    np.testing.assert_allclose(fd(Wd, lambda a: oracle.ffn_loss_f64(x, Wu, b, a, dy, l1)), gd, atol=1e-7)
+    np.testing.assert_allclose(fd(b, lambda a: oracle.ffn_loss_f64(x, Wu, a, Wd, dy, l1)), gb, atol=1e-7)
+    # dpre is dL/dpre: check it through the bias of one row at a time
+    assert np.allclose(dpre.sum(0), gb)
+
+
+def test_backward_matches_torch_autograd():
+    rng = np.random.default_rng(7)
+    M, d, F, l1 = 32, 48, 160, 1e-2
+    x = rng.standard_normal((M, d))
+    Wu = rng.standard_normal((F, d)) / math.sqrt(d)
+    Wd = rng.standard_normal((F, d)) / math.sqrt(F)
+    b = np.full(F, -1.0)
+    dy = rng.standard_normal((M, d))
+    L, h = oracle.ffn_loss_f64(x, Wu, b, Wd, dy, l1, want_h=True)
+    t = {k: torch.tensor(v, requires_grad=True) for k, v in dict(x=x, Wu=Wu, b=b, Wd=Wd).items()}
+    ht = torch.relu(t["x"] @ t["Wu"].T + t["b"])
+    Lt = (torch.tensor(dy) * (ht @ t["Wd"])).sum() + l1 * ht.abs().sum()
+    Lt.backward()
+    assert abs(Lt.item() - L) < 1e-9 * max(1.0, abs(L))
+    np.testing.assert_allclose(h, ht.detach().numpy(), rtol=0, atol=1e-12)
+    dpre, dx = oracle.ffn_bwd_rows(x, Wu, Wd, h, dy, l1)
+    gu, gd, gb = oracle.ffn_bwd_cols(x, Wu, Wd, h, dy, l1)
+    np.testing.assert_allclose(dx, t["x"].grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gu, t["Wu"].grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gd, t["Wd"].grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gb, t["b"].grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_backward_row_and_column_subsets_agree_with_full():
+    x, Wu, b, Wd, dy, l1 = _fd_setup(seed=3, M=9, d=5, F=12)
+    _, h = oracle.ffn_loss_f64(x, Wu, b, Wd, dy, l1, want_h=True)
+    dpre, dx = oracle.ffn_bwd_rows(x, Wu, Wd, h, dy, l1)
+    rows = np.array([8, 2, 5], np.int32)
+    dpre_s, dx_s = oracle.ffn_bwd_rows(x, Wu, Wd, h, dy, l1, rows=rows)
+    np.testing.assert_array_equal(dpre_s, dpre[rows])
+    np.testing.assert_array_equal(dx_s, dx[rows])
+    gu, gd, gb = oracle.ffn_bwd_cols(x, Wu, Wd, h, dy, l1)
+    cols = np.array([11, 0, 6], np.int32)
+    gus, gds, gbs = oracle.ffn_bwd_cols(x, Wu, Wd, h, dy, l1, cols=cols)
+    np.testing.assert_array_equal(gus, gu[cols])
+    np.testing.assert_array_equal(gds, gd[cols])
+    np.testing.assert_array_equal(gbs, gb[cols])
+
+
+def test_generator_is_counter_based_and_seeded():
+    a = syn.normal(0, syn.STREAM_X, 1000)
+    b = syn.normal(0, syn.STREAM_X, 1000)
+    np.testing.assert_array_equal(a, b)
+    c = syn.normal(1, syn.STREAM_X, 1000)
+    assert not np.array_equal(a, c)
+    u = syn.uniform(0, 3, 2000)
+    np.testing.assert_array_equal(syn.uniform(0, 3, 500, start=1500), u[1500:])
+    assert abs(a.mean()) < 0.15 and abs(a.std() - 1) < 0.1
+    np.testing.assert_array_equal(syn.to_bf16_bits(a.astype(np.float32)),
+                                  _torch_bf16_bits(a.astype(np.float32)))
