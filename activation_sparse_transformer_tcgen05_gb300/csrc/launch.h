@@ -1,0 +1,83 @@
+// launch.h — host-side launchers of the TwELL kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace twell {
+
+// Device view of a TwELL (same fields as the public twell_buf).
+struct TwellView {
+    int M, F, T, n_tiles;
+    int64_t cap;
+    int32_t* nnz;
+    int32_t* K;
+    int64_t* off;
+    int32_t* idx;
+    uint16_t* val;
+};
+
+// ---- TwELL construction (twell_sparse.cu)
+// nnz[r] of a dense bf16 matrix.
+cudaError_t launch_count_dense(const uint16_t* h, int ldh, const TwellView& tw, int32_t* status, cudaStream_t s);
+// K[t] = max nnz over tile t, off[] = compact prefix; capacity check.
+cudaError_t launch_tile_layout(const TwellView& tw, int32_t* status, cudaStream_t s);
+// Slots from a dense bf16 matrix.
+cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, int32_t* status, cudaStream_t s);
+// Slots from GEMM-epilogue staging. ReLU staging: uint32 (bf16 << 16 | local col);
+// gate staging: uint2 (global col, fp32 gate bits) and gate values go to gval[slot].
+cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
+                                    const TwellView& tw, int32_t* status, cudaStream_t s);
+cudaError_t launch_fill_staged_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
+                                    const TwellView& tw, float* gval, int32_t* status, cudaStream_t s);
+
+// ---- Sparse products (twell_sparse.cu)
+// y[r,:] = sum_k v[r,k] * W[idx[r,k], :]; v is the TwELL's bf16 val (vals_f32 == nullptr)
+// or an fp32 array indexed by slot.
+cudaError_t launch_spmm_rows(const TwellView& tw, const float* vals_f32, const uint16_t* W, int d,
+                             uint16_t* y, int32_t* status, cudaStream_t s);
+// dpre[slot] = dy[r] . W[idx] + l1 on stored slots, 0 on padding.
+cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float l1,
+                         float* dpre, int32_t* status, cudaStream_t s);
+// Gated: val[slot] = bf16(relu(g) * (x[r] . W_up[idx])) on stored slots.
+cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16_t* W_up, int d,
+                            const float* gval, int32_t* status, cudaStream_t s);
+
+// ---- Column lists (CSC) of a TwELL, rows ascending inside a column
+struct CscWork {
+    int row_blocks, rows_per_block;
+    unsigned long long* masks;  // [row_blocks, F]
+    int32_t* start;             // [row_blocks, F]
+    int32_t* colcnt;            // [F]
+    int32_t* colptr;            // [F + 1]
+    int32_t* crow;              // [cap]
+    int32_t* cslot;             // [cap]
+};
+void csc_plan(int M, int F, int* row_blocks, int* rows_per_block);
+cudaError_t launch_csc(const TwellView& tw, const CscWork& w, int32_t* status, cudaStream_t s);
+// dW_down[j] = sum h dy[r], dW_up[j] = sum dpre x[r], db[j] = sum dpre over column j.
+cudaError_t launch_wgrad(const TwellView& tw, const CscWork& w, const float* dpre, const uint16_t* x,
+                         const uint16_t* dy, int d, float* dW_up, float* dW_down, float* db, int32_t* status,
+                         cudaStream_t s);
+
+// ---- tcgen05 GEMM (twell_gemm.cu)
+enum GemmMode { GEMM_TWELL_RELU = 0, GEMM_GATE_SWAP = 1, GEMM_DENSE = 2 };
+struct GemmArgs {
+    int rowsA, rowsB, K;   // A [rowsA, K], B [rowsB, K], both bf16 K-major
+    const float* bias;     // TWELL_RELU: per B row; GATE_SWAP: per A row; DENSE: per B row or null
+    int relu;              // DENSE only
+    uint32_t* stage;       // TWELL_RELU staging [rowsA, NB, BN]
+    uint2* gstage;         // GATE_SWAP staging [rowsB, NB, 128]
+    int32_t* stage_cnt;    // [rows, NB]
+    int32_t* nnz;          // [rows], zeroed by the caller before the launch
+    int NB;                // column blocks of the staging
+    uint16_t* out;         // DENSE output [rowsA, ldo]
+    int ldo;
+    int32_t* status;
+};
+// Returns the column-block width BN the GEMM uses for this mode/shape.
+int gemm_block_n(int mode, int rowsB);
+cudaError_t launch_gemm(int mode, const uint16_t* A, const uint16_t* B, const GemmArgs& a, int sm_count,
+                        cudaStream_t s);
+
+}  // namespace twell

@@ -1,0 +1,317 @@
+// twell_api.cu — the C ABI declared in include/twell.h: argument checks,
+// workspace carving and the kernel sequence of each entry point. No entry
+// point allocates, frees or synchronises (except twell_check).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/twell.h"
+#include "launch.h"
+
+using namespace twell;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int sm_count_current()
+{
+    static int cached[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Workspace carving: consecutive 256-byte-aligned regions.
+struct Carver {
+    char* base;
+    size_t used = 0;
+    template <typename T>
+    T* take(size_t count)
+    {
+        T* p = reinterpret_cast<T*>(base ? base + used : nullptr);
+        used = round_up(used + count * sizeof(T), 256);
+        return p;
+    }
+};
+
+constexpr int kReluBN = 256;  // column block of the ReLU GEMM epilogue
+constexpr int kGateBM = 128;  // hidden-unit block of the gate GEMM epilogue
+
+struct FwdWs {
+    int32_t* stage_cnt;
+    uint32_t* stage;
+    uint2* gstage;
+    float* gval;
+};
+
+size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out)
+{
+    Carver c{static_cast<char*>(ws)};
+    FwdWs w{};
+    if (!gated) {
+        const size_t NB = (F + kReluBN - 1) / kReluBN;
+        w.stage_cnt = c.take<int32_t>((size_t)M * NB);
+        w.stage = c.take<uint32_t>((size_t)M * NB * kReluBN);
+    } else {
+        const size_t NB = (F + kGateBM - 1) / kGateBM;
+        w.stage_cnt = c.take<int32_t>((size_t)M * NB);
+        w.gstage = c.take<uint2>((size_t)M * NB * kGateBM);
+        w.gval = c.take<float>((size_t)(cap > 0 ? cap : 1));
+    }
+    if (out) *out = w;
+    return c.used;
+}
+
+struct BwdWs {
+    float* dpre;
+    CscWork csc;
+};
+
+size_t carve_bwd(void* ws, int M, int F, int64_t cap, BwdWs* out)
+{
+    Carver c{static_cast<char*>(ws)};
+    BwdWs w{};
+    csc_plan(M, F, &w.csc.row_blocks, &w.csc.rows_per_block);
+    const size_t capn = (size_t)(cap > 0 ? cap : 1);
+    w.dpre = c.take<float>(capn);
+    w.csc.masks = c.take<unsigned long long>((size_t)w.csc.row_blocks * F);
+    w.csc.start = c.take<int32_t>((size_t)w.csc.row_blocks * F);
+    w.csc.colcnt = c.take<int32_t>((size_t)F);
+    w.csc.colptr = c.take<int32_t>((size_t)F + 1);
+    w.csc.crow = c.take<int32_t>(capn);
+    w.csc.cslot = c.take<int32_t>(capn);
+    if (out) *out = w;
+    return c.used;
+}
+
+twell_status check_buf(const twell_buf* b, int M, int F, int T)
+{
+    if (!b) return TWELL_ERR_INVALID_ARG;
+    if (b->M != M || b->F != F || b->T != T || T <= 0) return TWELL_ERR_INVALID_ARG;
+    if (b->n_tiles != (M + T - 1) / T || b->cap_slots < 0) return TWELL_ERR_INVALID_ARG;
+    if (!b->nnz_row || !b->K_tile || !b->tile_off) return TWELL_ERR_INVALID_ARG;
+    if (b->cap_slots > 0 && (!b->idx || !b->val)) return TWELL_ERR_INVALID_ARG;
+    return TWELL_OK;
+}
+
+TwellView view_of(const twell_buf* b)
+{
+    TwellView v;
+    v.M = b->M;
+    v.F = b->F;
+    v.T = b->T;
+    v.n_tiles = b->n_tiles;
+    v.cap = b->cap_slots;
+    v.nnz = b->nnz_row;
+    v.K = b->K_tile;
+    v.off = b->tile_off;
+    v.idx = b->idx;
+    v.val = b->val;
+    return v;
+}
+
+twell_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA; }
+
+bool dims_ok(int M, int d, int F) { return M > 0 && d > 0 && F > 0 && d % 8 == 0 && F % 8 == 0; }
+
+// Limits of this build's kernels.
+constexpr int kMaxD = 4096;      // row dot products keep 16 chunks of 256 columns per warp in registers
+constexpr int kMaxFBwd = 28672;  // per-block column masks of the backward live in shared memory
+
+}  // namespace
+
+extern "C" {
+
+const char* twell_status_string(int status)
+{
+    switch (status) {
+        case TWELL_OK: return "ok";
+        case TWELL_ERR_INVALID_ARG: return "invalid argument";
+        case TWELL_ERR_UNSUPPORTED: return "unsupported shape or mode";
+        case TWELL_ERR_WORKSPACE: return "workspace too small";
+        case TWELL_ERR_CAPACITY: return "TwELL capacity exceeded";
+        case TWELL_ERR_TIMEOUT: return "bounded device wait expired";
+        case TWELL_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int64_t twell_buf_slots_bound(int M, int F, int T)
+{
+    if (M <= 0 || F <= 0 || T <= 0) return -1;
+    return (int64_t)M * (int64_t)F;
+}
+
+size_t twell_workspace_bytes(int op, int M, int d, int F, int T, int64_t cap_slots)
+{
+    (void)d;
+    (void)T;
+    if (M <= 0 || F <= 0) return 0;
+    switch (op) {
+        case TWELL_OP_FFN_FWD: return carve_fwd(nullptr, false, M, F, cap_slots, nullptr);
+        case TWELL_OP_GATED_FWD: return carve_fwd(nullptr, true, M, F, cap_slots, nullptr);
+        case TWELL_OP_FFN_BWD: return carve_bwd(nullptr, M, F, cap_slots, nullptr);
+        default: return 0;
+    }
+}
+
+int twell_device_sm_count(void) { return sm_count_current(); }
+
+twell_status twell_pack(const uint16_t* h, int M, int F, int ldh, int T, const twell_buf* out, int32_t* status,
+                        void* stream)
+{
+    if (!h || !status || M <= 0 || F <= 0 || F % 8 != 0 || ldh < F || ldh % 8 != 0 || !aligned16(h))
+        return TWELL_ERR_INVALID_ARG;
+    twell_status st = check_buf(out, M, F, T);
+    if (st != TWELL_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const TwellView tw = view_of(out);
+    cudaError_t e = launch_count_dense(h, ldh, tw, status, s);
+    if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
+    if (e == cudaSuccess) e = launch_fill_dense(h, ldh, tw, status, s);
+    return cuda_status(e);
+}
+
+twell_status twell_spmm_down(const twell_buf* h, const uint16_t* W_down, int d, uint16_t* y, int32_t* status,
+                             void* stream)
+{
+    if (!h || !W_down || !y || !status || d <= 0 || d % 8 != 0 || !aligned16(W_down) || !aligned16(y))
+        return TWELL_ERR_INVALID_ARG;
+    if (h->M <= 0 || h->F <= 0) return TWELL_ERR_INVALID_ARG;
+    twell_status st = check_buf(h, h->M, h->F, h->T);
+    if (st != TWELL_OK) return st;
+    const TwellView tw = view_of(h);
+    return cuda_status(launch_spmm_rows(tw, nullptr, W_down, d, y, status, static_cast<cudaStream_t>(stream)));
+}
+
+twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b,
+                           const uint16_t* W_down, int M, int d, int F, int T, const twell_buf* h_out, uint16_t* y,
+                           void* ws, size_t ws_bytes, int32_t* status, void* stream)
+{
+    if (!x || !W_up || !b || !W_down || !y || !status || !dims_ok(M, d, F)) return TWELL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(y) || (W_gate && !aligned16(W_gate)))
+        return TWELL_ERR_INVALID_ARG;
+    twell_status st = check_buf(h_out, M, F, T);
+    if (st != TWELL_OK) return st;
+    const bool gated = W_gate != nullptr;
+    if (gated && d > kMaxD) return TWELL_ERR_UNSUPPORTED;
+    const size_t need = carve_fwd(nullptr, gated, M, F, h_out->cap_slots, nullptr);
+    if (!ws || ws_bytes < need) return TWELL_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;
+    const int sms = sm_count_current();
+    if (sms <= 0) return TWELL_ERR_CUDA;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const TwellView tw = view_of(h_out);
+    FwdWs w;
+    carve_fwd(ws, gated, M, F, h_out->cap_slots, &w);
+    cudaError_t e = cudaMemsetAsync(tw.nnz, 0, sizeof(int32_t) * (size_t)M, s);
+    GemmArgs ga{};
+    ga.K = d;
+    ga.bias = b;
+    ga.stage_cnt = w.stage_cnt;
+    ga.nnz = tw.nnz;
+    ga.status = status;
+    if (!gated) {
+        ga.rowsA = M;
+        ga.rowsB = F;
+        ga.stage = w.stage;
+        ga.NB = (F + kReluBN - 1) / kReluBN;
+        if (e == cudaSuccess) e = launch_gemm(GEMM_TWELL_RELU, x, W_up, ga, sms, s);
+        if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
+        if (e == cudaSuccess) e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, status, s);
+    } else {
+        ga.rowsA = F;
+        ga.rowsB = M;
+        ga.gstage = w.gstage;
+        ga.NB = (F + kGateBM - 1) / kGateBM;
+        if (e == cudaSuccess) e = launch_gemm(GEMM_GATE_SWAP, W_gate, x, ga, sms, s);
+        if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
+        if (e == cudaSuccess)
+            e = launch_fill_staged_gate(w.gstage, w.stage_cnt, ga.NB, kGateBM, tw, w.gval, status, s);
+        if (e == cudaSuccess) e = launch_gated_up(tw, x, W_up, d, w.gval, status, s);
+    }
+    if (e == cudaSuccess) e = launch_spmm_rows(tw, nullptr, W_down, d, y, status, s);
+    return cuda_status(e);
+}
+
+twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down, const twell_buf* h,
+                           const uint16_t* dy, int d, float l1_coef, uint16_t* dx, float* dW_up, float* dW_down,
+                           float* db, void* ws, size_t ws_bytes, int32_t* status, void* stream)
+{
+    if (!x || !W_up || !W_down || !h || !dy || !dx || !dW_up || !dW_down || !db || !status)
+        return TWELL_ERR_INVALID_ARG;
+    const int M = h->M, F = h->F;
+    if (!dims_ok(M, d, F)) return TWELL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(dy) || !aligned16(dx) ||
+        !aligned16(dW_up) || !aligned16(dW_down))
+        return TWELL_ERR_INVALID_ARG;
+    twell_status st = check_buf(h, M, F, h->T);
+    if (st != TWELL_OK) return st;
+    if (d > kMaxD || F > kMaxFBwd || h->cap_slots >= (int64_t)INT32_MAX) return TWELL_ERR_UNSUPPORTED;
+    const size_t need = carve_bwd(nullptr, M, F, h->cap_slots, nullptr);
+    if (!ws || ws_bytes < need) return TWELL_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const TwellView tw = view_of(h);
+    BwdWs w;
+    carve_bwd(ws, M, F, h->cap_slots, &w);
+    cudaError_t e = launch_sddmm(tw, dy, W_down, d, l1_coef, w.dpre, status, s);
+    if (e == cudaSuccess) e = launch_spmm_rows(tw, w.dpre, W_up, d, dx, status, s);
+    if (e == cudaSuccess) e = launch_csc(tw, w.csc, status, s);
+    if (e == cudaSuccess) e = launch_wgrad(tw, w.csc, w.dpre, x, dy, d, dW_up, dW_down, db, status, s);
+    return cuda_status(e);
+}
+
+twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const float* b, const uint16_t* W_downT,
+                                 int M, int d, int F, uint16_t* h_dense, uint16_t* y, int32_t* status, void* stream)
+{
+    if (!x || !W_up || !W_downT || !h_dense || !y || !status || !dims_ok(M, d, F)) return TWELL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_up) || !aligned16(W_downT) || !aligned16(h_dense) || !aligned16(y))
+        return TWELL_ERR_INVALID_ARG;
+    const int sms = sm_count_current();
+    if (sms <= 0) return TWELL_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmArgs g1{};
+    g1.rowsA = M;
+    g1.rowsB = F;
+    g1.K = d;
+    g1.bias = b;
+    g1.relu = 1;
+    g1.out = h_dense;
+    g1.ldo = F;
+    g1.status = status;
+    cudaError_t e = launch_gemm(GEMM_DENSE, x, W_up, g1, sms, s);
+    GemmArgs g2{};
+    g2.rowsA = M;
+    g2.rowsB = d;
+    g2.K = F;
+    g2.bias = nullptr;
+    g2.relu = 0;
+    g2.out = y;
+    g2.ldo = d;
+    g2.status = status;
+    if (e == cudaSuccess) e = launch_gemm(GEMM_DENSE, h_dense, W_downT, g2, sms, s);
+    return cuda_status(e);
+}
+
+twell_status twell_check(const int32_t* status, void* stream, int32_t* host_status)
+{
+    if (!status || !host_status) return TWELL_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TWELL_ERR_CUDA;
+    if (cudaMemcpy(host_status, status, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TWELL_ERR_CUDA;
+    return TWELL_OK;
+}
+
+}  // extern "C"

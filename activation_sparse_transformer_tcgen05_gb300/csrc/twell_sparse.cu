@@ -1,0 +1,739 @@
+// twell_sparse.cu — TwELL construction, sparse products and the sparse backward.
+//
+// The method ("Sparser, Faster, Lighter Transformer Language Models", Resumo
+// Técnico §2 Metodologia) packs the ReLU hidden matrix into TwELL and runs the
+// down-projection and the training kernels only over the stored entries. These
+// are the CUDA-core kernels of that path: every one is a gather over rows of a
+// dense bf16 matrix (W_down, W_up, x or dy) named by TwELL indices, with fp32
+// accumulation. Work is split so that a warp's 32 lanes read one 512-byte
+// stretch of a gathered row with 128-bit loads; all reductions run in a fixed
+// order, so results are bit-reproducible.
+#include "common.cuh"
+#include "launch.h"
+
+namespace twell {
+
+namespace {
+
+constexpr int kWarps = 8;  // warps per block of the sparse kernels
+
+__device__ __forceinline__ int warp_sum_i(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_max_i(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum_f(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_incl_scan(int v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+__device__ __forceinline__ int nz_bf16(uint32_t half) { return (half & 0x7fffu) != 0u; }
+
+// First slot of row r and its tile width.
+__device__ __forceinline__ int64_t row_base(const TwellView& tw, int r, int* Kt)
+{
+    const int t = r / tw.T;
+    *Kt = tw.K[t];
+    return tw.off[t] + (int64_t)(r - t * tw.T) * (*Kt);
+}
+
+// acc[0..7] += v * (8 bf16 in w)
+__device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w)
+{
+    acc[0] = fmaf(v, bf16_lo(w.x), acc[0]);
+    acc[1] = fmaf(v, bf16_hi(w.x), acc[1]);
+    acc[2] = fmaf(v, bf16_lo(w.y), acc[2]);
+    acc[3] = fmaf(v, bf16_hi(w.y), acc[3]);
+    acc[4] = fmaf(v, bf16_lo(w.z), acc[4]);
+    acc[5] = fmaf(v, bf16_hi(w.z), acc[5]);
+    acc[6] = fmaf(v, bf16_lo(w.w), acc[6]);
+    acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
+}
+
+// sum_k a[k] * b[k] over 8 bf16 pairs
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& b)
+{
+    float s = bf16_lo(a.x) * bf16_lo(b.x);
+    s = fmaf(bf16_hi(a.x), bf16_hi(b.x), s);
+    s = fmaf(bf16_lo(a.y), bf16_lo(b.y), s);
+    s = fmaf(bf16_hi(a.y), bf16_hi(b.y), s);
+    s = fmaf(bf16_lo(a.z), bf16_lo(b.z), s);
+    s = fmaf(bf16_hi(a.z), bf16_hi(b.z), s);
+    s = fmaf(bf16_lo(a.w), bf16_lo(b.w), s);
+    s = fmaf(bf16_hi(a.w), bf16_hi(b.w), s);
+    return s;
+}
+
+__device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+__device__ __forceinline__ float load_val(const float* vals_f32, const uint16_t* val_bf16, int64_t s)
+{
+    return vals_f32 ? vals_f32[s] : bf16_to_f32(val_bf16[s]);
+}
+
+__device__ __forceinline__ bool over_capacity(const TwellView& tw)
+{
+    return tw.off[tw.n_tiles] > tw.cap;
+}
+
+// ------------------------------------------------------------ construction --
+
+// nnz[r] = number of entries of row r of a dense bf16 matrix that are not +-0.
+__global__ void k_count_dense(const uint16_t* __restrict__ h, int ldh, TwellView tw, const int32_t* status)
+{
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= tw.M || has_error(status)) return;
+    const uint16_t* row = h + (size_t)r * ldh;
+    int c = 0;
+    for (int j = lane * 8; j < tw.F; j += 256) {
+        const uint4 q = ldg16(row + j);
+        c += nz_bf16(q.x) + nz_bf16(q.x >> 16) + nz_bf16(q.y) + nz_bf16(q.y >> 16) + nz_bf16(q.z) +
+             nz_bf16(q.z >> 16) + nz_bf16(q.w) + nz_bf16(q.w >> 16);
+    }
+    c = warp_sum_i(c);
+    if (lane == 0) tw.nnz[r] = c;
+}
+
+// One block of 1024 threads: K[t] = max nnz over tile t (a warp per tile), then
+// off[] = exclusive prefix of rows(t) * K[t]; flags a capacity overflow.
+__global__ void __launch_bounds__(1024) k_tile_layout(TwellView tw, int32_t* status)
+{
+    __shared__ int64_t s_chunk[1024];
+    __shared__ int64_t s_warp[32];
+    __shared__ int64_t s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (has_error(status)) return;
+    if (tid == 0) {
+        s_carry = 0;
+        tw.off[0] = 0;
+    }
+    __syncthreads();
+    for (int t0 = 0; t0 < tw.n_tiles; t0 += 1024) {
+        const int chunk = min(1024, tw.n_tiles - t0);
+        for (int tt = warp; tt < chunk; tt += 32) {
+            const int t = t0 + tt, r0 = t * tw.T, rows = min(tw.T, tw.M - r0);
+            int mx = 0;
+            for (int i = lane; i < rows; i += 32) mx = max(mx, tw.nnz[r0 + i]);
+            mx = warp_max_i(mx);
+            if (lane == 0) {
+                tw.K[t] = mx;
+                s_chunk[tt] = (int64_t)rows * mx;
+            }
+        }
+        __syncthreads();
+        int64_t v = tid < chunk ? s_chunk[tid] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t n = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += n;
+        }
+        if (lane == 31) s_warp[warp] = v;
+        __syncthreads();
+        if (warp == 0) {
+            int64_t w = s_warp[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int64_t n = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += n;
+            }
+            s_warp[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int64_t incl = v + (warp > 0 ? s_warp[warp - 1] : 0);
+        if (tid < chunk) tw.off[t0 + tid + 1] = s_carry + incl;
+        __syncthreads();
+        if (tid == 0) s_carry += s_warp[31];
+        __syncthreads();
+    }
+    if (tid == 0 && s_carry > tw.cap) set_error(status, TWELL_ERR_CAPACITY);
+}
+
+// Slots of row r (a warp) from a dense bf16 matrix: warp prefix-sum order keeps
+// the columns ascending; padding (-1, +0) after the row's entries.
+__global__ void k_fill_dense(const uint16_t* __restrict__ h, int ldh, TwellView tw, const int32_t* status)
+{
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
+    int Kt;
+    const int64_t base = row_base(tw, r, &Kt);
+    const uint16_t* row = h + (size_t)r * ldh;
+    int pos = 0;
+    for (int j0 = 0; j0 < tw.F; j0 += 256) {
+        const int j = j0 + lane * 8;
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (j < tw.F) q = ldg16(row + j);
+        const uint32_t e[4] = {q.x, q.y, q.z, q.w};
+        int c = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c += nz_bf16(e[k]) + nz_bf16(e[k] >> 16);
+        const int incl = warp_incl_scan(c, lane);
+        int64_t p = base + pos + (incl - c);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t hv = (e[k >> 1] >> ((k & 1) * 16)) & 0xffffu;
+            if (nz_bf16(hv)) {
+                tw.idx[p] = j + k;
+                tw.val[p] = (uint16_t)hv;
+                ++p;
+            }
+        }
+        pos += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    for (int k = pos + lane; k < Kt; k += 32) {
+        tw.idx[base + k] = -1;
+        tw.val[base + k] = 0;
+    }
+}
+
+// Slots of row r (a warp) from the up-projection epilogue's staging: the row's
+// column blocks are concatenated in block order (each block's entries are
+// already ascending), then padded.
+__global__ void k_fill_staged_relu(const uint32_t* __restrict__ stage, const int32_t* __restrict__ stage_cnt, int NB,
+                                   int BN, TwellView tw, const int32_t* status)
+{
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
+    int Kt;
+    const int64_t base = row_base(tw, r, &Kt);
+    int pos = 0;
+    for (int nb0 = 0; nb0 < NB; nb0 += 32) {
+        const int nb = nb0 + lane;
+        const int c = nb < NB ? stage_cnt[(size_t)r * NB + nb] : 0;
+        const int incl = warp_incl_scan(c, lane);
+        const int64_t p = base + pos + (incl - c);
+        const uint32_t* src = stage + ((size_t)r * NB + nb) * BN;
+        for (int e = 0; e < c; ++e) {
+            const uint32_t w = src[e];
+            tw.idx[p + e] = nb * BN + (int)(w & 0xffffu);
+            tw.val[p + e] = (uint16_t)(w >> 16);
+        }
+        pos += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    for (int k = pos + lane; k < Kt; k += 32) {
+        tw.idx[base + k] = -1;
+        tw.val[base + k] = 0;
+    }
+}
+
+// Same for the gate staging: entries (global column, fp32 gate value). The
+// values go to gval[slot]; val[] is written later by the gated-up kernel.
+__global__ void k_fill_staged_gate(const uint2* __restrict__ stage, const int32_t* __restrict__ stage_cnt, int NB,
+                                   int BM, TwellView tw, float* gval, const int32_t* status)
+{
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
+    int Kt;
+    const int64_t base = row_base(tw, r, &Kt);
+    int pos = 0;
+    for (int nb0 = 0; nb0 < NB; nb0 += 32) {
+        const int nb = nb0 + lane;
+        const int c = nb < NB ? stage_cnt[(size_t)r * NB + nb] : 0;
+        const int incl = warp_incl_scan(c, lane);
+        const int64_t p = base + pos + (incl - c);
+        const uint2* src = stage + ((size_t)r * NB + nb) * BM;
+        for (int e = 0; e < c; ++e) {
+            const uint2 w = src[e];
+            tw.idx[p + e] = (int)w.x;
+            gval[p + e] = __uint_as_float(w.y);
+        }
+        pos += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    for (int k = pos + lane; k < Kt; k += 32) {
+        tw.idx[base + k] = -1;
+        tw.val[base + k] = 0;
+        gval[base + k] = 0.f;
+    }
+}
+
+// -------------------------------------------------------- sparse products --
+
+// y[r, cols] = sum_k v[r,k] W[idx[r,k], cols] for one (row, 256-column group)
+// task. SPLIT warps share a task, each taking a contiguous share of the row's
+// entries; their partial sums are added in warp order through shared memory.
+template <int SPLIT>
+__global__ void __launch_bounds__(kWarps * 32) k_spmm_rows(TwellView tw, const float* __restrict__ vals_f32,
+                                                           const uint16_t* __restrict__ W, int d,
+                                                           uint16_t* __restrict__ y, const int32_t* status)
+{
+    __shared__ float red[SPLIT > 1 ? kWarps : 1][SPLIT > 1 ? 256 : 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ngroups = (d + 255) >> 8;
+    const int64_t task = (int64_t)blockIdx.x * (kWarps / SPLIT) + warp / SPLIT;
+    const int sub = warp % SPLIT;
+    if (has_error(status) || over_capacity(tw)) return;  // uniform across the block
+    const int r = (int)(task / ngroups), g = (int)(task % ngroups);
+    const bool task_ok = r < tw.M;
+    const int c0 = g * 256 + lane * 8;
+    const bool col_ok = task_ok && c0 < d;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    if (task_ok) {
+        int Kt;
+        const int64_t base = row_base(tw, r, &Kt);
+        const int n = tw.nnz[r];
+        const int per = (n + SPLIT - 1) / SPLIT;
+        const int kb = min(n, sub * per), ke = min(n, kb + per);
+        const uint16_t* Wc = W + c0;
+        for (int k0 = kb; k0 < ke; k0 += 32) {
+            const int m = min(32, ke - k0);
+            int jl = 0;
+            float vl = 0.f;
+            if (lane < m) {
+                jl = tw.idx[base + k0 + lane];
+                vl = load_val(vals_f32, tw.val, base + k0 + lane);
+            }
+            int u = 0;
+            for (; u + 4 <= m; u += 4) {
+                const int j0 = __shfl_sync(0xffffffffu, jl, u), j1 = __shfl_sync(0xffffffffu, jl, u + 1);
+                const int j2 = __shfl_sync(0xffffffffu, jl, u + 2), j3 = __shfl_sync(0xffffffffu, jl, u + 3);
+                const float v0 = __shfl_sync(0xffffffffu, vl, u), v1 = __shfl_sync(0xffffffffu, vl, u + 1);
+                const float v2 = __shfl_sync(0xffffffffu, vl, u + 2), v3 = __shfl_sync(0xffffffffu, vl, u + 3);
+                if (col_ok) {
+                    const uint4 w0 = ldg16(Wc + (size_t)j0 * d), w1 = ldg16(Wc + (size_t)j1 * d);
+                    const uint4 w2 = ldg16(Wc + (size_t)j2 * d), w3 = ldg16(Wc + (size_t)j3 * d);
+                    fma8(acc, v0, w0);
+                    fma8(acc, v1, w1);
+                    fma8(acc, v2, w2);
+                    fma8(acc, v3, w3);
+                }
+            }
+            for (; u < m; ++u) {
+                const int j0 = __shfl_sync(0xffffffffu, jl, u);
+                const float v0 = __shfl_sync(0xffffffffu, vl, u);
+                if (col_ok) fma8(acc, v0, ldg16(Wc + (size_t)j0 * d));
+            }
+        }
+    }
+    if constexpr (SPLIT > 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) red[warp][lane * 8 + e] = acc[e];
+        __syncthreads();
+        if (sub != 0) return;
+        for (int s2 = 1; s2 < SPLIT; ++s2) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += red[warp + s2][lane * 8 + e];
+        }
+    }
+    if (col_ok) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(y + (size_t)r * d + c0) = o;
+    }
+}
+
+// Row dot products on the stored entries: for entry (r, k) with column j,
+// s = A[r] . W[j]. MODE 0 (backward SDDMM): out[slot] = s + l1 on stored slots
+// and 0 on padding. MODE 1 (gated up): val[slot] = bf16(g * s), g = gval[slot].
+// WPR warps share a row, entry k going to warp k % WPR; a row's A slice stays
+// in registers (NCH chunks of 256 columns, 8 per lane).
+template <int NCH, int MODE>
+__global__ void __launch_bounds__(kWarps * 32) k_row_dots(TwellView tw, const uint16_t* __restrict__ A,
+                                                          const uint16_t* __restrict__ W, int d, int wpr, float l1,
+                                                          float* __restrict__ out, const float* __restrict__ gval,
+                                                          const int32_t* status)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (kWarps / wpr) + warp / wpr;
+    const int sub = warp % wpr;
+    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
+    uint4 a[NCH];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        const int c = ch * 256 + lane * 8;
+        a[ch] = c < d ? ldg16(A + (size_t)r * d + c) : make_uint4(0, 0, 0, 0);
+    }
+    int Kt;
+    const int64_t base = row_base(tw, r, &Kt);
+    const int n = tw.nnz[r];
+    // entries of this warp: k = sub + wpr * q, q = 0, 1, ...
+    const int nq = n > sub ? (n - sub + wpr - 1) / wpr : 0;
+    for (int q0 = 0; q0 < nq; q0 += 32) {
+        const int m = min(32, nq - q0);
+        const int kl = sub + wpr * (q0 + lane);
+        const int jl = lane < m ? tw.idx[base + kl] : 0;
+        float res = 0.f;
+        int u = 0;
+        for (; u + 2 <= m; u += 2) {
+            const int ja = __shfl_sync(0xffffffffu, jl, u), jb = __shfl_sync(0xffffffffu, jl, u + 1);
+            float sa = 0.f, sb = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                const int c = ch * 256 + lane * 8;
+                if (c < d) {
+                    const uint4 wa = ldg16(W + (size_t)ja * d + c);
+                    const uint4 wb = ldg16(W + (size_t)jb * d + c);
+                    sa += dot8(a[ch], wa);
+                    sb += dot8(a[ch], wb);
+                }
+            }
+            sa = warp_sum_f(sa);
+            sb = warp_sum_f(sb);
+            if (lane == u) res = sa;
+            if (lane == u + 1) res = sb;
+        }
+        if (u < m) {
+            const int ja = __shfl_sync(0xffffffffu, jl, u);
+            float sa = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                const int c = ch * 256 + lane * 8;
+                if (c < d) sa += dot8(a[ch], ldg16(W + (size_t)ja * d + c));
+            }
+            sa = warp_sum_f(sa);
+            if (lane == u) res = sa;
+        }
+        if (lane < m) {
+            const int64_t s = base + kl;
+            if (MODE == 0) {
+                out[s] = res + l1;
+            } else {
+                tw.val[s] = f32_to_bf16_bits(fmaxf(gval[s], 0.f) * res);
+            }
+        }
+    }
+    if (MODE == 0 && sub == 0) {
+        for (int k = n + lane; k < Kt; k += 32) out[base + k] = 0.f;
+    }
+}
+
+// ------------------------------------------------------------- CSC build ----
+//
+// Column lists of the stored entries, rows ascending inside each column, built
+// without atomics on global memory: row blocks of 64 rows record, per column,
+// a 64-bit mask of the rows that hold it; a column-wise scan of the mask
+// popcounts gives each (block, column) its start, and an entry's position is
+// colptr[j] + start[b][j] + popcount of the mask bits below its row.
+
+constexpr int kCscRows = 64;
+
+__global__ void __launch_bounds__(256) k_csc_mask(TwellView tw, unsigned long long* __restrict__ masks,
+                                                  const int32_t* status)
+{
+    extern __shared__ unsigned long long s_mask[];  // [F]
+    const int b = blockIdx.x;
+    if (has_error(status)) return;
+    for (int j = threadIdx.x; j < tw.F; j += blockDim.x) s_mask[j] = 0ull;
+    __syncthreads();
+    const int r0 = b * kCscRows, r1 = min(tw.M, r0 + kCscRows);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r = r0 + warp; r < r1; r += blockDim.x >> 5) {
+        int Kt;
+        const int64_t base = row_base(tw, r, &Kt);
+        const int n = tw.nnz[r];
+        const unsigned long long bit = 1ull << (r - r0);
+        for (int k = lane; k < n; k += 32) atomicOr(&s_mask[tw.idx[base + k]], bit);
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < tw.F; j += blockDim.x) masks[(size_t)b * tw.F + j] = s_mask[j];
+}
+
+// 32 columns per block: start[b][j] = sum over blocks b' < b of popc(mask[b'][j]);
+// colcnt[j] = total over all blocks.
+__global__ void __launch_bounds__(1024) k_csc_colscan(const unsigned long long* __restrict__ masks, int row_blocks,
+                                                      int F, int32_t* __restrict__ start, int32_t* __restrict__ colcnt,
+                                                      const int32_t* status)
+{
+    __shared__ int s_cnt[32][33];
+    __shared__ int s_carry[32];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 32
+    const int j = blockIdx.x * 32 + tx;
+    if (has_error(status)) return;
+    if (ty == 0) s_carry[tx] = 0;
+    __syncthreads();
+    for (int b0 = 0; b0 < row_blocks; b0 += 32) {
+        const int b = b0 + ty;
+        s_cnt[ty][tx] = (b < row_blocks && j < F) ? __popcll(masks[(size_t)b * F + j]) : 0;
+        __syncthreads();
+        // warp ty scans column (blockIdx.x*32 + ty) over the 32 blocks (lane = block)
+        const int v = s_cnt[tx][ty];
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (tx >= o) incl += n;
+        }
+        const int jj = blockIdx.x * 32 + ty;
+        const int bb = b0 + tx;
+        const int carry = s_carry[ty];
+        if (jj < F && bb < row_blocks) start[(size_t)bb * F + jj] = carry + incl - v;
+        __syncthreads();
+        if (tx == 31) s_carry[ty] = carry + incl;
+        __syncthreads();
+    }
+    if (ty == 0 && j < F) colcnt[j] = s_carry[tx];
+}
+
+// Single block: ptr[0..n] = exclusive prefix of cnt[0..n).
+__global__ void __launch_bounds__(1024) k_scan_i32(const int32_t* __restrict__ cnt, int n, int32_t* __restrict__ ptr,
+                                                   const int32_t* status)
+{
+    __shared__ int s_warp[32];
+    __shared__ int s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (has_error(status)) return;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += 1024) {
+        const int i = i0 + tid;
+        const int v = i < n ? cnt[i] : 0;
+        int incl = warp_incl_scan(v, lane);
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) s_warp[lane] = warp_incl_scan(s_warp[lane], lane);
+        __syncthreads();
+        incl += (warp > 0 ? s_warp[warp - 1] : 0);
+        if (i < n) ptr[i] = s_carry + incl - v;
+        __syncthreads();
+        if (tid == 0) s_carry += s_warp[31];
+        __syncthreads();
+    }
+    if (tid == 0) ptr[n] = s_carry;
+}
+
+__global__ void k_csc_scatter(TwellView tw, const unsigned long long* __restrict__ masks,
+                              const int32_t* __restrict__ start, const int32_t* __restrict__ colptr,
+                              int32_t* __restrict__ crow, int32_t* __restrict__ cslot, const int32_t* status)
+{
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= tw.M || has_error(status)) return;
+    int Kt;
+    const int64_t base = row_base(tw, r, &Kt);
+    const int n = tw.nnz[r];
+    const int b = r / kCscRows;
+    const unsigned long long below = (1ull << (r - b * kCscRows)) - 1ull;
+    for (int k = lane; k < n; k += 32) {
+        const int j = tw.idx[base + k];
+        const size_t bj = (size_t)b * tw.F + j;
+        const int pos = colptr[j] + start[bj] + __popcll(masks[bj] & below);
+        crow[pos] = r;
+        cslot[pos] = (int32_t)(base + k);
+    }
+}
+
+// Weight gradients, one warp per (hidden unit j, 256-column group):
+// dW_down[j] = sum_e h_e dy[r_e], dW_up[j] = sum_e dpre_e x[r_e] over the
+// column's entries in row order; db[j] by the group-0 warp.
+__global__ void __launch_bounds__(kWarps * 32) k_wgrad(TwellView tw, const int32_t* __restrict__ colptr,
+                                                       const int32_t* __restrict__ crow,
+                                                       const int32_t* __restrict__ cslot,
+                                                       const float* __restrict__ dpre,
+                                                       const uint16_t* __restrict__ x,
+                                                       const uint16_t* __restrict__ dy, int d,
+                                                       float* __restrict__ dW_up, float* __restrict__ dW_down,
+                                                       float* __restrict__ db, const int32_t* status)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ngroups = (d + 255) >> 8;
+    const int64_t task = (int64_t)blockIdx.x * kWarps + warp;
+    const int j = (int)(task / ngroups), g = (int)(task % ngroups);
+    if (j >= tw.F || has_error(status)) return;
+    const int c0 = g * 256 + lane * 8;
+    const bool col_ok = c0 < d;
+    float ad[8], au[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ad[e] = au[e] = 0.f;
+    float bsum = 0.f;
+    const int e0 = colptr[j], e1 = colptr[j + 1];
+    for (int b0 = e0; b0 < e1; b0 += 32) {
+        const int m = min(32, e1 - b0);
+        int rl = 0;
+        float hl = 0.f, pl = 0.f;
+        if (lane < m) {
+            rl = crow[b0 + lane];
+            const int s = cslot[b0 + lane];
+            hl = bf16_to_f32(tw.val[s]);
+            pl = dpre[s];
+        }
+        bsum += pl;
+        int u = 0;
+        for (; u + 2 <= m; u += 2) {
+            const int ra = __shfl_sync(0xffffffffu, rl, u), rb = __shfl_sync(0xffffffffu, rl, u + 1);
+            const float ha = __shfl_sync(0xffffffffu, hl, u), hb = __shfl_sync(0xffffffffu, hl, u + 1);
+            const float pa = __shfl_sync(0xffffffffu, pl, u), pb = __shfl_sync(0xffffffffu, pl, u + 1);
+            if (col_ok) {
+                const uint4 dya = ldg16(dy + (size_t)ra * d + c0), xa = ldg16(x + (size_t)ra * d + c0);
+                const uint4 dyb = ldg16(dy + (size_t)rb * d + c0), xb = ldg16(x + (size_t)rb * d + c0);
+                fma8(ad, ha, dya);
+                fma8(au, pa, xa);
+                fma8(ad, hb, dyb);
+                fma8(au, pb, xb);
+            }
+        }
+        if (u < m) {
+            const int ra = __shfl_sync(0xffffffffu, rl, u);
+            const float ha = __shfl_sync(0xffffffffu, hl, u), pa = __shfl_sync(0xffffffffu, pl, u);
+            if (col_ok) {
+                fma8(ad, ha, ldg16(dy + (size_t)ra * d + c0));
+                fma8(au, pa, ldg16(x + (size_t)ra * d + c0));
+            }
+        }
+    }
+    if (col_ok) {
+        float4* pd = reinterpret_cast<float4*>(dW_down + (size_t)j * d + c0);
+        float4* pu = reinterpret_cast<float4*>(dW_up + (size_t)j * d + c0);
+        pd[0] = make_float4(ad[0], ad[1], ad[2], ad[3]);
+        pd[1] = make_float4(ad[4], ad[5], ad[6], ad[7]);
+        pu[0] = make_float4(au[0], au[1], au[2], au[3]);
+        pu[1] = make_float4(au[4], au[5], au[6], au[7]);
+    }
+    if (g == 0) {
+        bsum = warp_sum_f(bsum);
+        if (lane == 0) db[j] = bsum;
+    }
+}
+
+inline unsigned grid_for_warps(int64_t warps) { return (unsigned)((warps + kWarps - 1) / kWarps); }
+
+}  // namespace
+
+// ------------------------------------------------------------- launchers ----
+
+cudaError_t launch_count_dense(const uint16_t* h, int ldh, const TwellView& tw, int32_t* status, cudaStream_t s)
+{
+    k_count_dense<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(h, ldh, tw, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tile_layout(const TwellView& tw, int32_t* status, cudaStream_t s)
+{
+    k_tile_layout<<<1, 1024, 0, s>>>(tw, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, int32_t* status, cudaStream_t s)
+{
+    k_fill_dense<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(h, ldh, tw, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
+                                    const TwellView& tw, int32_t* status, cudaStream_t s)
+{
+    k_fill_staged_relu<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(stage, stage_cnt, NB, BN, tw, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_staged_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
+                                    const TwellView& tw, float* gval, int32_t* status, cudaStream_t s)
+{
+    k_fill_staged_gate<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(stage, stage_cnt, NB, BM, tw, gval, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_spmm_rows(const TwellView& tw, const float* vals_f32, const uint16_t* W, int d, uint16_t* y,
+                             int32_t* status, cudaStream_t s)
+{
+    const int64_t tasks = (int64_t)tw.M * ((d + 255) / 256);
+    if (tw.M >= 256) {
+        k_spmm_rows<1><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
+    } else {
+        k_spmm_rows<8><<<(unsigned)tasks, kWarps * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
+    }
+    return cudaGetLastError();
+}
+
+template <int MODE>
+static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const uint16_t* W, int d, float l1,
+                                   float* out, const float* gval, int32_t* status, cudaStream_t s)
+{
+    const int nch = (d + 255) / 256;
+    const int wpr = tw.M >= 256 ? 1 : kWarps;
+    const unsigned grid = (unsigned)(((int64_t)tw.M * wpr + kWarps - 1) / kWarps);
+#define TWELL_ROWDOT_CASE(N)                                                                      \
+    case N:                                                                                       \
+        k_row_dots<N, MODE><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, l1, out, gval, status); \
+        break;
+    switch (nch) {
+        TWELL_ROWDOT_CASE(1)
+        TWELL_ROWDOT_CASE(2)
+        TWELL_ROWDOT_CASE(3)
+        TWELL_ROWDOT_CASE(4)
+        TWELL_ROWDOT_CASE(5)
+        TWELL_ROWDOT_CASE(6)
+        TWELL_ROWDOT_CASE(7)
+        TWELL_ROWDOT_CASE(8)
+        TWELL_ROWDOT_CASE(12)
+        TWELL_ROWDOT_CASE(16)
+        default:
+            if (nch <= 12) {
+                k_row_dots<12, MODE><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, l1, out, gval, status);
+            } else if (nch <= 16) {
+                k_row_dots<16, MODE><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, l1, out, gval, status);
+            } else {
+                return cudaErrorInvalidValue;
+            }
+    }
+#undef TWELL_ROWDOT_CASE
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float l1, float* dpre,
+                         int32_t* status, cudaStream_t s)
+{
+    return launch_row_dots<0>(tw, dy, W, d, l1, dpre, nullptr, status, s);
+}
+
+cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16_t* W_up, int d, const float* gval,
+                            int32_t* status, cudaStream_t s)
+{
+    return launch_row_dots<1>(tw, x, W_up, d, 0.f, nullptr, gval, status, s);
+}
+
+void csc_plan(int M, int F, int* row_blocks, int* rows_per_block)
+{
+    (void)F;
+    *rows_per_block = kCscRows;
+    *row_blocks = (M + kCscRows - 1) / kCscRows;
+}
+
+cudaError_t launch_csc(const TwellView& tw, const CscWork& w, int32_t* status, cudaStream_t s)
+{
+    const size_t smem = (size_t)tw.F * sizeof(unsigned long long);
+    cudaError_t e = cudaFuncSetAttribute(k_csc_mask, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_csc_mask<<<w.row_blocks, 256, smem, s>>>(tw, w.masks, status);
+    k_csc_colscan<<<(tw.F + 31) / 32, 1024, 0, s>>>(w.masks, w.row_blocks, tw.F, w.start, w.colcnt, status);
+    k_scan_i32<<<1, 1024, 0, s>>>(w.colcnt, tw.F, w.colptr, status);
+    k_csc_scatter<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, w.masks, w.start, w.colptr, w.crow, w.cslot,
+                                                               status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wgrad(const TwellView& tw, const CscWork& w, const float* dpre, const uint16_t* x,
+                         const uint16_t* dy, int d, float* dW_up, float* dW_down, float* db, int32_t* status,
+                         cudaStream_t s)
+{
+    const int64_t tasks = (int64_t)tw.F * ((d + 255) / 256);
+    k_wgrad<<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, w.colptr, w.crow, w.cslot, dpre, x, dy, d, dW_up,
+                                                          dW_down, db, status);
+    return cudaGetLastError();
+}
+
+}  // namespace twell

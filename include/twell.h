@@ -1,0 +1,184 @@
+/*
+ * twell.h — C ABI of the TwELL activation-sparse feed-forward layer (sm_103a).
+ *
+ * The layer is the ReLU (or ReLU-gated) transformer feed-forward block of
+ * "Sparser, Faster, Lighter Transformer Language Models" (Cetin, Peluchetti,
+ * Castillo, Naruse, Murakami, Jones, 2026; gist.science summary, Resumo Técnico
+ * §2 Metodologia). L1-regularised training leaves more than 99 % of the hidden
+ * activations at zero; the post-ReLU hidden matrix h is packed into TwELL
+ * (Tile-wise ELLPACK) straight from the up-projection's epilogue, and the
+ * down-projection and the backward run only over the stored entries.
+ *
+ * TwELL layout (one tile = T consecutive token rows spanning all F hidden units):
+ *   nnz_row[r]   number of active entries of row r
+ *   K_tile[t]    max nnz_row over the rows of tile t (the tile's width)
+ *   tile_off[t]  first slot of tile t; tile_off[0] = 0,
+ *                tile_off[t+1] = tile_off[t] + rows(t) * K_tile[t],
+ *                rows(t) = min(T, M - t*T)
+ *   slot off[t] + i*K[t] + k of row i of tile t holds, for k < nnz, the k-th
+ *   active column in ascending order (idx, int32) and h there (val, bf16 bits);
+ *   for k >= nnz it holds idx = -1, val = +0.
+ * Active set: h != 0 for the ReLU layer and for twell_pack (-0 counts as zero,
+ * NaN as nonzero); pre_gate > 0 for the gated layer.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named in the argument list are DEVICE pointers unless marked
+ *     "host". bf16 tensors are passed as uint16_t bit arrays; all matrices are
+ *     row-major and densely packed (row stride = column count) unless a leading
+ *     dimension is given. Weights are [F, d]: one row per hidden unit.
+ *   - The caller owns and allocates every buffer. The library never allocates,
+ *     frees or synchronises (twell_check is the one call that synchronises);
+ *     each call only enqueues work on `stream` (a cudaStream_t passed as void*,
+ *     NULL = the legacy default stream) and returns. Buffers must stay alive
+ *     until that work has finished.
+ *   - Host-side argument errors are returned at once and nothing is enqueued.
+ *     Errors found on the device (capacity, bounded-wait timeout) are written
+ *     to `*status`, a caller-owned device int32 that the caller sets to 0
+ *     before the first call; the first nonzero code sticks and later kernels of
+ *     the same call skip their work. Read it after synchronising the stream, or
+ *     with twell_check().
+ *   - Alignment: every device pointer of a bf16 matrix must be 16-byte aligned
+ *     and d, F must be multiples of 8 (128-bit loads, TMA strides).
+ *   - All calls are deterministic: the same inputs give the same bits.
+ */
+#ifndef TWELL_H
+#define TWELL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum twell_status {
+    TWELL_OK = 0,
+    TWELL_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, misaligned pointer, bad d/F */
+    TWELL_ERR_UNSUPPORTED = 2, /* shape or mode this build does not implement */
+    TWELL_ERR_WORKSPACE = 3,   /* ws_bytes smaller than twell_workspace_bytes() */
+    TWELL_ERR_CAPACITY = 4,    /* device: TwELL needs more slots than cap_slots */
+    TWELL_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel expired */
+    TWELL_ERR_CUDA = 6         /* a CUDA runtime call or launch failed */
+} twell_status;
+
+/* Host struct describing one TwELL held in device memory (layout above).
+ * M, F, T, n_tiles = ceil(M/T) and cap_slots are set by the caller; the five
+ * device arrays are caller-allocated: nnz_row[M], K_tile[n_tiles],
+ * tile_off[n_tiles+1], idx[cap_slots], val[cap_slots]. */
+typedef struct twell_buf {
+    int32_t M, F, T, n_tiles;
+    int64_t cap_slots;
+    int32_t* nnz_row;
+    int32_t* K_tile;
+    int64_t* tile_off;
+    int32_t* idx;
+    uint16_t* val;
+} twell_buf;
+
+/* Operation codes for twell_workspace_bytes. */
+enum { TWELL_OP_PACK = 0, TWELL_OP_SPMM_DOWN = 1, TWELL_OP_FFN_FWD = 2,
+       TWELL_OP_FFN_BWD = 3, TWELL_OP_GATED_FWD = 4 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* twell_status_string(int status);
+
+/* Worst-case slot count of a TwELL of an M x F matrix with tile height T:
+ * M*F (every entry active). Returns -1 for non-positive sizes. */
+int64_t twell_buf_slots_bound(int M, int F, int T);
+
+/* Device workspace, in bytes, that `op` needs for these sizes. cap_slots is the
+ * TwELL capacity (used by TWELL_OP_FFN_BWD and TWELL_OP_GATED_FWD). 0 means
+ * none is needed. */
+size_t twell_workspace_bytes(int op, int M, int d, int F, int T, int64_t cap_slots);
+
+/* Number of streaming multiprocessors the library sizes its grids for. */
+int twell_device_sm_count(void);
+
+/*
+ * twell_pack — TwELL of a dense hidden matrix (the "Formato de Dados TwELL"
+ * paragraph of Resumo Técnico §2).
+ *   h      [M, ldh] bf16, entries (r, j < F) are read; ldh >= F, ldh % 8 == 0
+ *   out    host struct with out->M == M, out->F == F, out->T == T
+ * Writes nnz_row, K_tile, tile_off always; writes the slots only if
+ * tile_off[n_tiles] <= cap_slots, else sets *status = TWELL_ERR_CAPACITY.
+ */
+twell_status twell_pack(const uint16_t* h, int M, int F, int ldh, int T,
+                        const twell_buf* out, int32_t* status, void* stream);
+
+/*
+ * twell_spmm_down — y = h W_down over the stored entries of a TwELL (Resumo
+ * Técnico §2, "Kernels de Inferência": iterate only over the active neurons).
+ *   h       host struct of a valid TwELL (F rows of W_down are indexed)
+ *   W_down  [F, d] bf16
+ *   y       [M, d] bf16 output; fp32 accumulation, one rounding to bf16
+ */
+twell_status twell_spmm_down(const twell_buf* h, const uint16_t* W_down, int d,
+                             uint16_t* y, int32_t* status, void* stream);
+
+/*
+ * twell_ffn_fwd — the layer's forward pass.
+ *   ReLU  (W_gate == NULL): h = relu(x W_up^T + b), packed into TwELL inside the
+ *          tcgen05 up-projection's epilogue (Resumo Técnico §2: TwELL materialised
+ *          in the epilogue of the dense matmul), then y = h W_down.
+ *   Gated (W_gate != NULL): the gate GEMM x W_gate^T + b gives the active set and
+ *          is packed the same way; then for each active (r, j):
+ *          u = x[r] . W_up[j], h = bf16(relu(g) * u), y[r] += h W_down[j] (the
+ *          sparse up+down inference kernels of the same section).
+ *   x [M, d] bf16; W_up, W_gate, W_down [F, d] bf16; b [F] fp32 (added to the
+ *   ReLU pre-activation, or to the gate); y [M, d] bf16.
+ *   h_out: TwELL of h (M, F, T as given), its val holding h.
+ *   ws: device workspace of at least twell_workspace_bytes(TWELL_OP_FFN_FWD or
+ *   TWELL_OP_GATED_FWD, M, d, F, T, h_out->cap_slots) bytes, 256-byte aligned;
+ *   contents need no init. Gated mode limit of this build: d <= 4096.
+ * Capacity overflow of h_out: nnz/K/off are written, slots and y are not, and
+ * *status = TWELL_ERR_CAPACITY.
+ */
+twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate,
+                           const float* b, const uint16_t* W_down, int M, int d, int F, int T,
+                           const twell_buf* h_out, uint16_t* y, void* ws, size_t ws_bytes,
+                           int32_t* status, void* stream);
+
+/*
+ * twell_ffn_bwd — backward of L = <dy, y> + l1_coef * sum |h| for the ReLU
+ * layer (Resumo Técnico §2, "Técnicas de Treinamento": L1 on the ReLU
+ * activations), restricted to the stored entries of h:
+ *   dpre[r,j] = (dy[r] . W_down[j] + l1_coef) on active (r, j), 0 elsewhere
+ *   dx        = dpre W_up                       [M, d] bf16
+ *   dW_up     = dpre^T x                        [F, d] fp32 (every row written)
+ *   dW_down   = h^T dy                          [F, d] fp32 (every row written)
+ *   db        = column sums of dpre             [F]    fp32
+ *   x, dy [M, d] bf16; W_up, W_down [F, d] bf16; M and F are h->M and h->F.
+ *   h: the forward's TwELL; ws: at least twell_workspace_bytes(TWELL_OP_FFN_BWD,
+ *   M, d, F, T, h->cap_slots) bytes, 256-byte aligned. Limits of this build:
+ *   d <= 4096, F <= 28672, h->cap_slots < 2^31 (else TWELL_ERR_UNSUPPORTED).
+ * The reduction order of every sum is fixed (no floating-point atomics).
+ */
+twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down,
+                           const twell_buf* h, const uint16_t* dy, int d, float l1_coef,
+                           uint16_t* dx, float* dW_up, float* dW_down, float* db,
+                           void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
+/*
+ * twell_dense_ffn_fwd — the same ReLU layer computed densely with the same
+ * tcgen05 GEMM (a baseline for the sparse path, not part of the method):
+ *   h_dense = bf16(relu(x W_up^T + b))   [M, F] bf16 (written)
+ *   y       = h_dense W_down             [M, d] bf16
+ *   W_downT is W_down transposed, [d, F] bf16 (the dense GEMM reads both
+ *   operands K-major).
+ */
+twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const float* b,
+                                 const uint16_t* W_downT, int M, int d, int F,
+                                 uint16_t* h_dense, uint16_t* y, int32_t* status, void* stream);
+
+/*
+ * twell_check — synchronises `stream`, copies *status (device) to
+ * *host_status (host) and returns TWELL_OK, or TWELL_ERR_CUDA if the stream
+ * reported an error. This is the one entry point that synchronises.
+ */
+twell_status twell_check(const int32_t* status, void* stream, int32_t* host_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TWELL_H */

@@ -1,0 +1,316 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs. Bit-exact for the TwELL layout, 2e-2 * rms(ref) for
+floating-point outputs; see tests/helpers.py for the rules."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from helpers import (assert_close_rms, assert_twell_identical, bf16_f64, compare_hidden, dev_bf16, dev_f32,
+                     host_bf16_bits, preact_tau, status_tensor, twell_to_device, twell_to_host)
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from activation_sparse_transformer_tcgen05_gb300 import build as _build
+    _build.build()
+import activation_sparse_transformer_tcgen05_gb300 as tw  # noqa: E402
+
+
+def _status_ok(st):
+    code = tw.twell_check(st)
+    assert code == 0, f"device status {code}: {tw.twell_status_string(code)}"
+
+
+# ------------------------------------------------------------- twell_pack ---
+
+@pytest.mark.parametrize("M,F,T,density,skew,seed", [
+    (64, 512, 16, 0.01, 0.0, 0),       # tiny workload shape
+    (129, 264, 16, 0.05, 0.0, 1),      # ragged last tile, F not a multiple of 256
+    (37, 96, 1, 0.2, 0.0, 2),          # T = 1: per-row ELL
+    (50, 128, 200, 0.1, 0.0, 3),       # T >= M: classic ELL
+    (33, 64, 8, 1.0, 0.0, 4),          # everything active: K = F
+    (40, 256, 16, 0.0, 0.0, 5),        # nothing active: K = 0, no slots
+    (300, 1024, 128, 0.01, 1.0, 6),    # skewed row densities
+])
+def test_pack_bit_exact(M, F, T, density, skew, seed):
+    h = syn.sparse_hidden(M, F, density, seed=seed, row_skew_sigma=skew)
+    h[::5, ::7] = np.where(h[::5, ::7] == 0, np.uint16(0x8000), h[::5, ::7])  # -0.0 counts as zero
+    ref = oracle.twell_pack(h, T)
+    buf = tw.TwellBuffers(M, F, T, max(ref.slots, 1))
+    st = status_tensor()
+    tw.twell_pack(dev_bf16(h), T, buf, st)
+    _status_ok(st)
+    assert_twell_identical(twell_to_host(buf), ref)
+
+
+def test_pack_full_inference_size():
+    M, F, T = 4096, 8192, 128
+    h = syn.sparse_hidden(M, F, 0.0099, seed=7)
+    ref = oracle.twell_pack(h, T)
+    buf = tw.TwellBuffers(M, F, T, ref.slots)
+    st = status_tensor()
+    tw.twell_pack(dev_bf16(h), T, buf, st)
+    _status_ok(st)
+    assert_twell_identical(twell_to_host(buf), ref)
+
+
+def test_pack_capacity_overflow_reports_and_keeps_layout():
+    M, F, T = 64, 512, 16
+    h = syn.sparse_hidden(M, F, 0.05, seed=8)
+    ref = oracle.twell_pack(h, T)
+    buf = tw.TwellBuffers(M, F, T, ref.slots - 1)
+    st = status_tensor()
+    tw.twell_pack(dev_bf16(h), T, buf, st)
+    assert tw.twell_check(st) == 4  # TWELL_ERR_CAPACITY
+    np.testing.assert_array_equal(buf.nnz.cpu().numpy(), ref.nnz)
+    np.testing.assert_array_equal(buf.K.cpu().numpy(), ref.K)
+    np.testing.assert_array_equal(buf.off.cpu().numpy(), ref.off)
+
+
+# ------------------------------------------------------------- spmm down ----
+
+@pytest.mark.parametrize("M,F,d,T,density,seed", [
+    (64, 512, 128, 16, 0.01, 0),
+    (77, 264, 200, 8, 0.1, 1),     # ragged rows, d not a multiple of 256
+    (300, 1024, 512, 128, 0.02, 2),
+    (5, 64, 64, 1, 0.5, 3),
+])
+def test_spmm_down(M, F, d, T, density, seed):
+    h = syn.sparse_hidden(M, F, density, seed=seed)
+    W = syn.to_bf16_bits((syn.normal(seed, 9, F * d).reshape(F, d) / np.sqrt(F)).astype(np.float32))
+    ref_tw = oracle.twell_pack(h, T)
+    y_ref = oracle.twell_spmm(ref_tw, W)
+    buf = twell_to_device(ref_tw)
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    st = status_tensor()
+    tw.twell_spmm_down(buf, dev_bf16(W), y, st)
+    _status_ok(st)
+    assert_close_rms(bf16_f64(host_bf16_bits(y)), y_ref, what="y")
+
+
+def test_spmm_down_full_inference_size_sampled_rows():
+    M, F, d, T = 4096, 8192, 2048, 128
+    h = syn.sparse_hidden(M, F, 0.0099, seed=11)
+    W = syn.to_bf16_bits((syn.normal(11, 9, F * d).reshape(F, d) / np.sqrt(F)).astype(np.float32))
+    ref_tw = oracle.twell_pack(h, T)
+    buf = twell_to_device(ref_tw)
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    st = status_tensor()
+    tw.twell_spmm_down(buf, dev_bf16(W), y, st)
+    _status_ok(st)
+    rows = np.r_[0:3, 127:130, M - 3:M, np.random.default_rng(0).integers(0, M, 40)]
+    sub = oracle.Twell(len(rows), F, 1, *_rows_twell(ref_tw, rows))
+    y_ref = oracle.twell_spmm(sub, W)
+    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], y_ref, what="y rows")
+
+
+def _rows_twell(tw_, rows):
+    """Per-row (T = 1) TwELL of selected rows of a TwELL, for the oracle."""
+    nnz, K, off, idx, val = [], [], [0], [], []
+    for r in rows:
+        t, i = divmod(int(r), tw_.T)
+        base = tw_.off[t] + i * tw_.K[t]
+        n = int(tw_.nnz[r])
+        nnz.append(n)
+        K.append(n)
+        idx.extend(tw_.idx[base:base + n])
+        val.extend(tw_.val[base:base + n])
+        off.append(off[-1] + n)
+    return (np.array(nnz, np.int32), np.array(K, np.int32), np.array(off, np.int64),
+            np.array(idx, np.int32), np.array(val, np.uint16))
+
+
+# ------------------------------------------------------- fused forward ------
+
+def _fwd(inp: syn.FFNInputs, cap=None):
+    M, d, F, T = inp.M, inp.d, inp.F, inp.T
+    cap = cap if cap is not None else M * F
+    buf = tw.TwellBuffers(M, F, T, cap)
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    gated = inp.W_gate is not None
+    op = tw.OP_GATED_FWD if gated else tw.OP_FFN_FWD
+    ws = torch.empty(tw.twell_workspace_bytes(op, M, d, F, T, cap), dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    tw.twell_ffn_fwd(dev_bf16(inp.x), dev_bf16(inp.W_up), None if not gated else dev_bf16(inp.W_gate),
+                     dev_f32(inp.b), dev_bf16(inp.W_down), T, buf, y, ws, st)
+    return buf, y, st
+
+
+def test_fwd_integer_inputs_bit_exact():
+    # integer-valued bf16 inputs: every fp32 partial sum is exact, so the TwELL
+    # and y (one rounding of an exact integer) must match the oracle bit for bit
+    inp = syn.integer_ffn_inputs(200, 128, 520, 16, seed=1, lo=-2, hi=2, bias=-9)
+    buf, y, st = _fwd(inp)
+    _status_ok(st)
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, inp.M, inp.d, inp.F)
+    assert ref["active"].mean() > 0.005
+    assert_twell_identical(twell_to_host(buf), oracle.twell_pack(ref["h"], inp.T))
+    np.testing.assert_array_equal(host_bf16_bits(y), oracle.round_bf16(ref["y"].astype(np.float32)))
+
+
+@pytest.mark.parametrize("M,d,F,T,bias,seed", [
+    (64, 128, 512, 16, -2.33, 0),      # the tiny workload
+    (200, 256, 1024, 128, -1.0, 1),    # several tiles, ragged last row tile
+    (130, 136, 264, 7, -0.5, 2),       # ragged K (d % 64 != 0), F % 256 != 0, odd T
+])
+def test_fwd_relu_matches_oracle(M, d, F, T, bias, seed):
+    inp = syn.ffn_inputs(M, d, F, T, bias, seed=seed)
+    buf, y, st = _fwd(inp)
+    _status_ok(st)
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F)
+    got = twell_to_host(buf)
+    code, h_gpu = oracle.twell_unpack(got)
+    assert code == 0, f"GPU TwELL violates the layout (code {code})"
+    tau = preact_tau(inp.x, inp.W_up, ref["pre"])
+    compare_hidden(h_gpu, ref["h"], h_gpu != 0, ref["active"] != 0, ref["pre"], tau)
+    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="y")
+
+
+def test_fwd_inference_full_size_sampled():
+    inp = syn.config_inputs("inference")
+    M, d, F, T = inp.M, inp.d, inp.F, inp.T
+    buf, y, st = _fwd(inp)
+    _status_ok(st)
+    got = twell_to_host(buf)
+    code, h_gpu = oracle.twell_unpack(got)
+    assert code == 0
+    rows = np.r_[0:2, 127:129, M - 2:M, np.random.default_rng(1).integers(0, M, 26)].astype(np.int32)
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, rows=rows)
+    tau = preact_tau(inp.x[rows], inp.W_up, ref["pre"])
+    compare_hidden(h_gpu[rows], ref["h"], h_gpu[rows] != 0, ref["active"] != 0, ref["pre"], tau)
+    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], ref["y"], what="y rows")
+    dens = got.nnz.sum() / (M * F)
+    assert 0.007 < dens < 0.013  # ~99 % sparse
+
+
+@pytest.mark.parametrize("name", ["decode1", "decode8", "decode64"])
+def test_fwd_gated_decode(name):
+    inp = syn.config_inputs(name)
+    M, d, F, T = inp.M, inp.d, inp.F, inp.T
+    buf, y, st = _fwd(inp)
+    _status_ok(st)
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, inp.W_gate, inp.b, inp.W_down, M, d, F)
+    got = twell_to_host(buf)
+    # the stored set is the gate's support; values are h = bf16(relu(g) * u)
+    act_gpu = np.zeros((M, F), bool)
+    h_gpu = np.zeros((M, F), np.uint16)
+    for r in range(M):
+        t, i = divmod(r, T)
+        base = got.off[t] + i * got.K[t]
+        cols = got.idx[base:base + got.nnz[r]]
+        assert np.all(np.diff(cols) > 0)
+        act_gpu[r, cols] = True
+        h_gpu[r, cols] = got.val[base:base + got.nnz[r]]
+    tau = preact_tau(inp.x, inp.W_gate, ref["pre"])
+    diff = act_gpu != (ref["active"] != 0)
+    assert not (diff & (np.abs(ref["pre"]) > tau)).any()
+    both = act_gpu & (ref["active"] != 0)
+    assert_close_rms(bf16_f64(h_gpu)[both], bf16_f64(ref["h"])[both], what="gated h")
+    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="y")
+
+
+def test_fwd_capacity_overflow():
+    inp = syn.ffn_inputs(64, 128, 512, 16, -1.0, seed=3)
+    buf, y, st = _fwd(inp, cap=8)
+    assert tw.twell_check(st) == 4
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, 64, 128, 512)
+    nnz = buf.nnz.cpu().numpy()
+    assert abs(int(nnz.sum()) - int((ref["active"] != 0).sum())) <= 4
+
+
+def test_fwd_workspace_too_small_is_rejected_on_host():
+    inp = syn.ffn_inputs(64, 128, 512, 16, -2.33, seed=0)
+    buf = tw.TwellBuffers(64, 512, 16, 64 * 512)
+    y = torch.empty(64, 128, dtype=torch.int16, device="cuda")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tw.TwellError) as e:
+        tw.twell_ffn_fwd(dev_bf16(inp.x), dev_bf16(inp.W_up), None, dev_f32(inp.b), dev_bf16(inp.W_down), 16,
+                         buf, y, ws, status_tensor())
+    assert e.value.status == 3
+
+
+# ------------------------------------------------------------- backward -----
+
+def _bwd(x, W_up, W_down, ref_tw, dy, l1):
+    M, d = x.shape
+    F = W_up.shape[0]
+    buf = twell_to_device(ref_tw)
+    dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    db = torch.empty(F, dtype=torch.float32, device="cuda")
+    ws = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, ref_tw.T, buf.cap_slots),
+                     dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    tw.twell_ffn_bwd(dev_bf16(x), dev_bf16(W_up), dev_bf16(W_down), buf, dev_bf16(dy), l1, dx, dWu, dWd, db, ws, st)
+    _status_ok(st)
+    return bf16_f64(host_bf16_bits(dx)), dWu.cpu().numpy(), dWd.cpu().numpy(), db.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,d,F,T,bias,l1,seed", [
+    (64, 128, 512, 16, -2.33, 1e-4, 0),
+    (150, 264, 520, 32, -1.5, 0.0, 1),
+    (90, 64, 1024, 128, -1.0, 5e-2, 2),
+])
+def test_bwd_matches_oracle(M, d, F, T, bias, l1, seed):
+    inp = syn.ffn_inputs(M, d, F, T, bias, seed=seed, with_dy=True)
+    fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, want_y=False)
+    ref_tw = oracle.twell_pack(fw["h"], T)
+    dx, dWu, dWd, db = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, l1)
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, fw["h"], inp.dy))
+    _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1)
+    assert_close_rms(dx, dx_ref, what="dx")
+    assert_close_rms(dWu, gu, what="dW_up")
+    assert_close_rms(dWd, gd, what="dW_down")
+    assert_close_rms(db, gb, what="db")
+    unused = np.flatnonzero((fw["h"] != 0).sum(0) == 0)
+    assert np.all(dWu[unused] == 0) and np.all(dWd[unused] == 0) and np.all(db[unused] == 0)
+
+
+def test_bwd_inference_size_sampled():
+    M, d, F, T, l1 = 4096, 2048, 8192, 128, 1e-4
+    h = syn.sparse_hidden(M, F, 0.0099, seed=21)
+    inp = syn.ffn_inputs(M, d, F, T, -2.33, seed=21, with_dy=True)
+    ref_tw = oracle.twell_pack(h, T)
+    dx, dWu, dWd, db = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, l1)
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, h, inp.dy))
+    rng = np.random.default_rng(5)
+    rows = np.r_[0, M - 1, rng.integers(0, M, 14)].astype(np.int32)
+    cols = np.r_[0, F - 1, rng.integers(0, F, 14)].astype(np.int32)
+    _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1, rows=rows)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1, cols=cols)
+    assert_close_rms(dx[rows], dx_ref, what="dx rows")
+    assert_close_rms(dWu[cols], gu, what="dW_up cols")
+    assert_close_rms(dWd[cols], gd, what="dW_down cols")
+    assert_close_rms(db[cols], gb, what="db cols")
+
+
+def test_bwd_is_deterministic():
+    inp = syn.ffn_inputs(128, 256, 512, 32, -1.5, seed=4, with_dy=True)
+    fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, 128, 256, 512, want_y=False)
+    ref_tw = oracle.twell_pack(fw["h"], 32)
+    a = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, 1e-3)
+    b = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, 1e-3)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
+
+
+# ------------------------------------------------------ dense baseline ------
+
+@pytest.mark.parametrize("M,d,F", [(64, 128, 512), (200, 264, 520)])
+def test_dense_baseline_matches_oracle(M, d, F):
+    inp = syn.ffn_inputs(M, d, F, 16, -1.0, seed=6)
+    h = torch.empty(M, F, dtype=torch.int16, device="cuda")
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    WdT = np.ascontiguousarray(inp.W_down.T)
+    st = status_tensor()
+    tw.twell_dense_ffn_fwd(dev_bf16(inp.x), dev_bf16(inp.W_up), dev_f32(inp.b), dev_bf16(WdT), h, y, st)
+    _status_ok(st)
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F)
+    hg = host_bf16_bits(h)
+    tau = preact_tau(inp.x, inp.W_up, ref["pre"])
+    compare_hidden(hg, ref["h"], hg != 0, ref["active"] != 0, ref["pre"], tau)
+    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="dense y")
