@@ -4,7 +4,13 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace twell {
+
+// Kernels launched by this library in this process (read by twell_kernel_launches).
+extern std::atomic<long long> g_kernel_launches;
+inline void count_launches(int n) { g_kernel_launches.fetch_add(n, std::memory_order_relaxed); }
 
 // Device view of a TwELL (same fields as the public twell_buf).
 struct TwellView {

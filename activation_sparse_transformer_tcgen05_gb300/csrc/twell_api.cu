@@ -192,13 +192,12 @@ twell_status twell_spmm_down(const twell_buf* h, const uint16_t* W_down, int d, 
     return cuda_status(launch_spmm_rows(tw, nullptr, W_down, d, y, status, static_cast<cudaStream_t>(stream)));
 }
 
-twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b,
-                           const uint16_t* W_down, int M, int d, int F, int T, const twell_buf* h_out, uint16_t* y,
-                           void* ws, size_t ws_bytes, int32_t* status, void* stream)
+twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b, int M,
+                           int d, int F, int T, const twell_buf* h_out, void* ws, size_t ws_bytes, int32_t* status,
+                           void* stream)
 {
-    if (!x || !W_up || !b || !W_down || !y || !status || !dims_ok(M, d, F)) return TWELL_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(y) || (W_gate && !aligned16(W_gate)))
-        return TWELL_ERR_INVALID_ARG;
+    if (!x || !W_up || !b || !status || !dims_ok(M, d, F)) return TWELL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_up) || (W_gate && !aligned16(W_gate))) return TWELL_ERR_INVALID_ARG;
     twell_status st = check_buf(h_out, M, F, T);
     if (st != TWELL_OK) return st;
     const bool gated = W_gate != nullptr;
@@ -239,8 +238,18 @@ twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16
             e = launch_fill_staged_gate(w.gstage, w.stage_cnt, ga.NB, kGateBM, tw, w.gval, status, s);
         if (e == cudaSuccess) e = launch_gated_up(tw, x, W_up, d, w.gval, status, s);
     }
-    if (e == cudaSuccess) e = launch_spmm_rows(tw, nullptr, W_down, d, y, status, s);
     return cuda_status(e);
+}
+
+twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b,
+                           const uint16_t* W_down, int M, int d, int F, int T, const twell_buf* h_out, uint16_t* y,
+                           void* ws, size_t ws_bytes, int32_t* status, void* stream)
+{
+    if (!W_down || !y || !aligned16(W_down) || !aligned16(y)) return TWELL_ERR_INVALID_ARG;
+    twell_status st = twell_up_pack(x, W_up, W_gate, b, M, d, F, T, h_out, ws, ws_bytes, status, stream);
+    if (st != TWELL_OK) return st;
+    const TwellView tw = view_of(h_out);
+    return cuda_status(launch_spmm_rows(tw, nullptr, W_down, d, y, status, static_cast<cudaStream_t>(stream)));
 }
 
 twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down, const twell_buf* h,
@@ -303,6 +312,8 @@ twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const 
     if (e == cudaSuccess) e = launch_gemm(GEMM_DENSE, h_dense, W_downT, g2, sms, s);
     return cuda_status(e);
 }
+
+int64_t twell_kernel_launches(void) { return (int64_t)g_kernel_launches.load(std::memory_order_relaxed); }
 
 twell_status twell_check(const int32_t* status, void* stream, int32_t* host_status)
 {

@@ -378,6 +378,7 @@ cudaError_t run(const uint16_t* A, const uint16_t* B, const GemmArgs& a, int tok
     if (e != cudaSuccess) return e;
     const int tiles = ((a.rowsA + BM - 1) / BM) * ((a.rowsB + BN - 1) / BN);
     const int grid = tiles < sm_count ? tiles : sm_count;
+    count_launches(1);
     kern<<<grid, 192, L::TOTAL, s>>>(ma, mb, a, tok0);
     return cudaGetLastError();
 }

@@ -13,6 +13,8 @@
 
 namespace twell {
 
+std::atomic<long long> g_kernel_launches{0};
+
 namespace {
 
 constexpr int kWarps = 8;  // warps per block of the sparse kernels
@@ -617,18 +619,21 @@ inline unsigned grid_for_warps(int64_t warps) { return (unsigned)((warps + kWarp
 
 cudaError_t launch_count_dense(const uint16_t* h, int ldh, const TwellView& tw, int32_t* status, cudaStream_t s)
 {
+    count_launches(1);
     k_count_dense<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(h, ldh, tw, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tile_layout(const TwellView& tw, int32_t* status, cudaStream_t s)
 {
+    count_launches(1);
     k_tile_layout<<<1, 1024, 0, s>>>(tw, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, int32_t* status, cudaStream_t s)
 {
+    count_launches(1);
     k_fill_dense<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(h, ldh, tw, status);
     return cudaGetLastError();
 }
@@ -636,6 +641,7 @@ cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, i
 cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
                                     const TwellView& tw, int32_t* status, cudaStream_t s)
 {
+    count_launches(1);
     k_fill_staged_relu<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(stage, stage_cnt, NB, BN, tw, status);
     return cudaGetLastError();
 }
@@ -643,6 +649,7 @@ cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_
 cudaError_t launch_fill_staged_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
                                     const TwellView& tw, float* gval, int32_t* status, cudaStream_t s)
 {
+    count_launches(1);
     k_fill_staged_gate<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(stage, stage_cnt, NB, BM, tw, gval, status);
     return cudaGetLastError();
 }
@@ -651,6 +658,7 @@ cudaError_t launch_spmm_rows(const TwellView& tw, const float* vals_f32, const u
                              int32_t* status, cudaStream_t s)
 {
     const int64_t tasks = (int64_t)tw.M * ((d + 255) / 256);
+    count_launches(1);
     if (tw.M >= 256) {
         k_spmm_rows<1><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
     } else {
@@ -666,6 +674,7 @@ static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const
     const int nch = (d + 255) / 256;
     const int wpr = tw.M >= 256 ? 1 : kWarps;
     const unsigned grid = (unsigned)(((int64_t)tw.M * wpr + kWarps - 1) / kWarps);
+    count_launches(1);
 #define TWELL_ROWDOT_CASE(N)                                                                      \
     case N:                                                                                       \
         k_row_dots<N, MODE><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, l1, out, gval, status); \
@@ -718,6 +727,7 @@ cudaError_t launch_csc(const TwellView& tw, const CscWork& w, int32_t* status, c
     const size_t smem = (size_t)tw.F * sizeof(unsigned long long);
     cudaError_t e = cudaFuncSetAttribute(k_csc_mask, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    count_launches(4);
     k_csc_mask<<<w.row_blocks, 256, smem, s>>>(tw, w.masks, status);
     k_csc_colscan<<<(tw.F + 31) / 32, 1024, 0, s>>>(w.masks, w.row_blocks, tw.F, w.start, w.colcnt, status);
     k_scan_i32<<<1, 1024, 0, s>>>(w.colcnt, tw.F, w.colptr, status);
@@ -731,6 +741,7 @@ cudaError_t launch_wgrad(const TwellView& tw, const CscWork& w, const float* dpr
                          cudaStream_t s)
 {
     const int64_t tasks = (int64_t)tw.F * ((d + 255) / 256);
+    count_launches(1);
     k_wgrad<<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, w.colptr, w.crow, w.cslot, dpre, x, dy, d, dW_up,
                                                           dW_down, db, status);
     return cudaGetLastError();

@@ -22,8 +22,8 @@ OP_PACK, OP_SPMM_DOWN, OP_FFN_FWD, OP_FFN_BWD, OP_GATED_FWD = 0, 1, 2, 3, 4
 # Every symbol include/twell.h declares.
 EXPORTED_SYMBOLS = (
     "twell_status_string", "twell_buf_slots_bound", "twell_workspace_bytes", "twell_device_sm_count",
-    "twell_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd", "twell_dense_ffn_fwd",
-    "twell_check",
+    "twell_pack", "twell_up_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd",
+    "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check",
 )
 
 
@@ -64,6 +64,9 @@ def load_library(path: str | None = None):
     lib.twell_device_sm_count.restype = I32
     lib.twell_pack.restype = I32
     lib.twell_pack.argtypes = [P, I32, I32, I32, I32, BUFP, P, P]
+    lib.twell_up_pack.restype = I32
+    lib.twell_up_pack.argtypes = [P, P, P, P, I32, I32, I32, I32, BUFP, P, SZ, P, P]
+    lib.twell_kernel_launches.restype = I64
     lib.twell_spmm_down.restype = I32
     lib.twell_spmm_down.argtypes = [BUFP, P, I32, P, P, P]
     lib.twell_ffn_fwd.restype = I32
@@ -153,6 +156,20 @@ def twell_pack(h: torch.Tensor, T: int, out: TwellBuffers, status: torch.Tensor,
     _check(load_library().twell_pack(ctypes.c_void_p(h.data_ptr()), M, F, h.stride(0), T, out.ref,
                                      _ptr(status, "status", bytes_per_elem=4), _stream(stream)),
            "twell_pack")
+
+
+def twell_kernel_launches() -> int:
+    return int(load_library().twell_kernel_launches())
+
+
+def twell_up_pack(x, W_up, W_gate, b, T: int, h_out: TwellBuffers, ws, status, stream=None):
+    M, d = x.shape
+    F = W_up.shape[0]
+    _check(load_library().twell_up_pack(
+        _ptr(x, "x", bytes_per_elem=2), _ptr(W_up, "W_up", bytes_per_elem=2, numel=F * d),
+        _ptr(W_gate, "W_gate", bytes_per_elem=2, numel=F * d), _ptr(b, "b", bytes_per_elem=4, numel=F),
+        M, d, F, T, h_out.ref, _ptr(ws, "ws"), ws.numel() * ws.element_size(),
+        _ptr(status, "status", bytes_per_elem=4), _stream(stream)), "twell_up_pack")
 
 
 def twell_spmm_down(h: TwellBuffers, W_down: torch.Tensor, y: torch.Tensor, status: torch.Tensor, stream=None):

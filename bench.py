@@ -1,0 +1,394 @@
+#!/usr/bin/env python
+"""Benchmark of the TwELL activation-sparse feed-forward hot path on one GB300.
+
+One step = the whole hot path over one batch of the inference workload
+(M=4096 tokens, d_model=2048, d_ff=8192, ReLU, bias -2.33 -> ~99 % of the hidden
+activations zero, TwELL tiles of 128 rows, L1 coefficient 1e-4, dy ~ N(0,1)):
+
+    twell_up_pack    tcgen05 up-projection, TwELL built in its epilogue (a1-a3)
+    twell_spmm_down  y = TwELL x W_down                                     (a4)
+    twell_ffn_bwd    dpre, dx, column lists, dW_up, dW_down, db             (a6-a9)
+
+Inputs are resident in HBM when the timed region starts; L2 is flushed (a
+512 MB write) between timed steps. Every stage is timed with CUDA events on the
+stream it runs on. Prints one JSON line (rank 0).
+
+--impl reference times the CPU oracle (plain C, fp64) on the host cores on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "sparse-FFN tokens/s fwd & fwd+bwd at 99% sparsity; % of HBM/tensor roofline"
+UNIT = "tokens/s"
+CONFIG_NAME = "inference"
+WORKLOAD = ("inference FFN layer: M=4096 tokens, d_model=2048, d_ff=8192, bf16, ReLU, bias=-2.33 "
+            "(~99% sparse), TwELL tile=128 rows, fp32 accumulation; step = fwd + bwd (dy~N(0,1), L1=1e-4)")
+L1 = 1e-4
+FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sust=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------- clock sampler --
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle --
+
+def oracle_step(inp: syn.FFNInputs, S: int):
+    """The oracle's fwd + bwd on the first S tokens of the workload (same weights)."""
+    import oracle
+    rows = np.arange(S, dtype=np.int32)
+    fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, inp.M, inp.d, inp.F, rows=rows)
+    X = oracle.bf16_to_f64(inp.x[:S])
+    DY = oracle.bf16_to_f64(inp.dy[:S])
+    H = oracle.bf16_to_f64(fw["h"])
+    Wu = oracle.bf16_to_f64(inp.W_up)
+    Wd = oracle.bf16_to_f64(inp.W_down)
+    oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, L1)
+    oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, L1)
+
+
+def oracle_rate(inp: syn.FFNInputs, budget_s: float):
+    """Tokens/s of the oracle on a sample sized to take about budget_s."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle_step(inp, 2)
+    t2 = time.perf_counter() - t0
+    S = int(max(1, min(inp.M, 2 * budget_s / max(t2, 1e-3))))
+    t0 = time.perf_counter()
+    oracle_step(inp, S)
+    dt = time.perf_counter() - t0
+    return S / dt, S, dt, oracle.num_threads()
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = syn.config_inputs(CONFIG_NAME, with_dy=True)
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    # size the per-step sample from a 2-token probe
+    t0 = time.perf_counter()
+    oracle_step(inp, 2)
+    t2 = time.perf_counter() - t0
+    S = int(max(1, min(inp.M, 2 * per_step / max(t2, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_step(inp, S)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(inp, S)
+        times.append(time.perf_counter() - t0)
+    ms = 1000.0 * statistics.mean(times)
+    value = S / (ms / 1000.0)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded splitmix64/Box-Muller)",
+        "config": {"workload": WORKLOAD, "sample_tokens_per_step": S},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"first {S} tokens of the workload per step, same weights (fwd + bwd)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU path ----
+
+def dev16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+class Layer:
+    def __init__(self, inp: syn.FFNInputs):
+        import activation_sparse_transformer_tcgen05_gb300 as tw
+        self.tw = tw
+        self.inp = inp
+        M, d, F, T = inp.M, inp.d, inp.F, inp.T
+        self.x, self.Wu, self.Wd, self.dy = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_down), dev16(inp.dy)
+        self.b = torch.from_numpy(inp.b).cuda()
+        self.cap = M * F
+        self.buf = tw.TwellBuffers(M, F, T, self.cap)
+        self.y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+        self.ws_f = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_FWD, M, d, F, T, self.cap), dtype=torch.uint8,
+                                device="cuda")
+        self.ws_b = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, self.cap), dtype=torch.uint8,
+                                device="cuda")
+        self.dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+        self.dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+        self.dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+        self.db = torch.empty(F, dtype=torch.float32, device="cuda")
+        self.st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def up(self):
+        self.tw.twell_up_pack(self.x, self.Wu, None, self.b, self.inp.T, self.buf, self.ws_f, self.st)
+
+    def down(self):
+        self.tw.twell_spmm_down(self.buf, self.Wd, self.y, self.st)
+
+    def bwd(self):
+        self.tw.twell_ffn_bwd(self.x, self.Wu, self.Wd, self.buf, self.dy, L1, self.dx, self.dWu, self.dWd,
+                              self.db, self.ws_b, self.st)
+
+
+def stage_roofline(name, ms, inp, slots, nnz, peaks):
+    M, d, F = inp.M, inp.d, inp.F
+    s = ms / 1000.0
+    if name == "up_pack":
+        flops = 2.0 * M * d * F
+        a = flops / s / 1e12
+        return {"bound": "tensor", "achieved": a, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": a / peaks["bf16"], "traffic": None,
+                "algorithmic": f"{flops / 1e9:.1f} GFLOP (2 M d_model d_ff)"}
+    if name == "spmm_down":
+        # compulsory: W_down once, the TwELL (idx + val) once, y written once
+        by = F * d * 2 + slots * 6 + M * d * 2 + M * 4
+    else:
+        # compulsory: x, dy, W_up, W_down, TwELL read once; dx, dW_up, dW_down, db written once
+        by = 2 * M * d * 2 + 2 * F * d * 2 + slots * 6 + M * d * 2 + 2 * F * d * 4 + F * 4
+    a = by / s / 1e9
+    return {"bound": "hbm", "achieved": a, "peak": peaks["hbm"], "unit": "GB/s", "frac": a / peaks["hbm"],
+            "traffic": None, "algorithmic": f"{by / 1e6:.1f} MB compulsory"}
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import activation_sparse_transformer_tcgen05_gb300 as tw
+    from activation_sparse_transformer_tcgen05_gb300 import build as tbuild
+    tbuild.build()
+    torch.cuda.set_device(local_rank)
+    peaks = _peaks()
+    inp = syn.config_inputs(CONFIG_NAME, with_dy=True)
+    L = Layer(inp)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(evs):
+        evs[0].record(stream)
+        L.up()
+        evs[1].record(stream)
+        L.down()
+        evs[2].record(stream)
+        L.bwd()
+        evs[3].record(stream)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xff)
+        step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    code = tw.twell_check(L.st)
+    if code != 0:
+        raise RuntimeError(f"device status {code}: {tw.twell_status_string(code)}")
+    slots = L.buf.slots()
+    nnz = int(L.buf.nnz.sum().item())
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.2)
+    launches0 = tw.twell_kernel_launches()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_((i + 7) & 0xff)
+        step(events[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = tw.twell_kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    code = tw.twell_check(L.st)
+    if code != 0:
+        raise RuntimeError(f"device status {code}: {tw.twell_status_string(code)}")
+
+    up = [e[0].elapsed_time(e[1]) for e in events]
+    down = [e[1].elapsed_time(e[2]) for e in events]
+    bwd = [e[2].elapsed_time(e[3]) for e in events]
+    ms = {"up_pack": statistics.mean(up), "spmm_down": statistics.mean(down), "ffn_bwd": statistics.mean(bwd)}
+    ms_step = sum(ms.values())
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * inp.M / (ms_step / 1000.0)
+    ms_fwd = ms["up_pack"] + ms["spmm_down"]
+
+    stages = {k: dict(ms=v, **stage_roofline(k, v, inp, slots, nnz, peaks)) for k, v in ms.items()}
+    dom = max(ms, key=ms.get)
+    roof = {k: stages[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["src"]
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if rank == 0 or True:
+        xh = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).pin_memory()
+        dyh = torch.from_numpy(np.ascontiguousarray(inp.dy).view(np.int16)).pin_memory()
+        yh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
+        dxh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
+        ke = max(3, min(args.steps, 50))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
+        for i in range(ke + 3):
+            flush.fill_(i & 0xff)
+            e = evs[i - 3] if i >= 3 else None
+            if e:
+                e[0].record(stream)
+            L.x.copy_(xh, non_blocking=True)
+            L.dy.copy_(dyh, non_blocking=True)
+            tw.twell_ffn_fwd(L.x, L.Wu, None, L.b, L.Wd, inp.T, L.buf, L.y, L.ws_f, L.st)
+            L.bwd()
+            yh.copy_(L.y, non_blocking=True)
+            dxh.copy_(L.dx, non_blocking=True)
+            if e:
+                e[1].record(stream)
+        torch.cuda.synchronize()
+        ems = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        e2e = {"value": world * inp.M / (ems / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": int(xh.numel() * 2 + dyh.numel() * 2),
+               "d2h_bytes_per_step": int(yh.numel() * 2 + dxh.numel() * 2), "ms_per_step": ems}
+
+    # ---- the build's own dense tcgen05 FFN forward on the same workload (context)
+    WdT = L.Wd.view(inp.F, inp.d).t().contiguous()
+    hd = torch.empty(inp.M, inp.F, dtype=torch.int16, device="cuda")
+    dts = []
+    for i in range(13):
+        flush.fill_(i & 0xff)
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        tw.twell_dense_ffn_fwd(L.x, L.Wu, L.b, WdT, hd, L.y, L.st)
+        b2.record(stream)
+        dts.append((a, b2))
+    torch.cuda.synchronize()
+    dense_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in dts[3:])
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, S, dt, cores = oracle_rate(inp, args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {S} of {inp.M} tokens, same weights, fwd + bwd, {dt:.1f} s"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, random-init weights)",
+        "config": {"workload": WORKLOAD, "M": inp.M, "d_model": inp.d, "d_ff": inp.F, "T": inp.T, "bias": -2.33,
+                   "l1": L1, "l2": "flushed between timed steps (512 MB write)",
+                   "parallelism": f"replicas x{world}", "measured_density": nnz / (inp.M * inp.F),
+                   "slots": slots},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "fwd": {"value": world * inp.M / (ms_fwd / 1000.0), "unit": UNIT, "ms": ms_fwd},
+        "stages": stages,
+        "dense_tcgen05_fwd_ms": dense_ms,
+        "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+    if world > 1 and args.impl == "ours":
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -106,6 +106,17 @@ twell_status twell_pack(const uint16_t* h, int M, int F, int ldh, int T,
                         const twell_buf* out, int32_t* status, void* stream);
 
 /*
+ * twell_up_pack — rows a1-a3 of the forward alone: the tcgen05 up (or gate)
+ * projection whose epilogue packs h into h_out, without the down-projection.
+ * Same arguments, workspace and error behaviour as twell_ffn_fwd minus W_down
+ * and y; in gated mode h_out's val holds h = bf16(relu(g) * u) on return.
+ * twell_ffn_fwd is exactly twell_up_pack followed by twell_spmm_down.
+ */
+twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate,
+                           const float* b, int M, int d, int F, int T, const twell_buf* h_out,
+                           void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
+/*
  * twell_spmm_down — y = h W_down over the stored entries of a TwELL (Resumo
  * Técnico §2, "Kernels de Inferência": iterate only over the active neurons).
  *   h       host struct of a valid TwELL (F rows of W_down are indexed)
@@ -169,6 +180,11 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
 twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const float* b,
                                  const uint16_t* W_downT, int M, int d, int F,
                                  uint16_t* h_dense, uint16_t* y, int32_t* status, void* stream);
+
+/* Number of kernels this library has launched in this process (host-side
+ * counter, all devices). Lets a caller count the library's launches in a
+ * timed region. */
+int64_t twell_kernel_launches(void);
 
 /*
  * twell_check — synchronises `stream`, copies *status (device) to

@@ -6,7 +6,11 @@ Comparison rules:
     bit-exact;
   * floating-point outputs (y, dx, dW_up, dW_down, db, gated h values):
     max |gpu - ref| <= 2e-2 * rms(ref), bf16 inputs with fp32 accumulation
-    against the fp64 oracle;
+    against the fp64 oracle. Outputs stored in bf16 (y, dx, gated h) are
+    compared with the oracle value rounded to bf16, and each element may also
+    differ by one bf16 ulp of itself: the fp32 and fp64 sums can round to
+    neighbouring bf16 values, and on heavy-tailed rows that single rounding
+    step exceeds 2e-2 * rms;
   * the hidden active set of the fused forward, where fp32 accumulation order
     decides a ReLU sign: an entry may differ from the oracle only where
     |pre_oracle| <= tau, tau = 2 * (gamma_d * sum_k |x_k w_k| + ulp32(pre)),
@@ -77,12 +81,29 @@ def assert_twell_identical(got: oracle.Twell, ref: oracle.Twell):
     np.testing.assert_array_equal(got.val, ref.val, err_msg="val")
 
 
-def assert_close_rms(got: np.ndarray, ref: np.ndarray, tol: float = RMS_TOL, what: str = ""):
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (8 significant bits)."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (np.maximum(e, -126) - 7), 2.0 ** -133)
+
+
+def assert_close_rms(got: np.ndarray, ref: np.ndarray, tol: float = RMS_TOL, what: str = "",
+                     bf16_out: bool = False):
+    """max|got - ref| <= tol * rms(ref); for bf16-stored outputs ref is rounded
+    to bf16 and one bf16 ulp of the element is allowed on top."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
-    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    if not ref.size:
+        return 0.0, 0.0
+    if bf16_out:
+        ref_q = oracle.bf16_to_f64(oracle.round_bf16(ref.astype(np.float32)))
+        excess = np.abs(got - ref_q) - bf16_ulp(ref_q)
+        err = float(np.max(excess))
+    else:
+        err = float(np.max(np.abs(got - ref)))
     assert err <= tol * rms + 1e-30, f"{what}: max|err| {err:.3e} > {tol} * rms {rms:.3e}"
     return err, rms
 

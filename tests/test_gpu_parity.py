@@ -87,7 +87,7 @@ def test_spmm_down(M, F, d, T, density, seed):
     st = status_tensor()
     tw.twell_spmm_down(buf, dev_bf16(W), y, st)
     _status_ok(st)
-    assert_close_rms(bf16_f64(host_bf16_bits(y)), y_ref, what="y")
+    assert_close_rms(bf16_f64(host_bf16_bits(y)), y_ref, what="y", bf16_out=True)
 
 
 def test_spmm_down_full_inference_size_sampled_rows():
@@ -103,7 +103,7 @@ def test_spmm_down_full_inference_size_sampled_rows():
     rows = np.r_[0:3, 127:130, M - 3:M, np.random.default_rng(0).integers(0, M, 40)]
     sub = oracle.Twell(len(rows), F, 1, *_rows_twell(ref_tw, rows))
     y_ref = oracle.twell_spmm(sub, W)
-    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], y_ref, what="y rows")
+    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], y_ref, what="y rows", bf16_out=True)
 
 
 def _rows_twell(tw_, rows):
@@ -165,7 +165,7 @@ def test_fwd_relu_matches_oracle(M, d, F, T, bias, seed):
     assert code == 0, f"GPU TwELL violates the layout (code {code})"
     tau = preact_tau(inp.x, inp.W_up, ref["pre"])
     compare_hidden(h_gpu, ref["h"], h_gpu != 0, ref["active"] != 0, ref["pre"], tau)
-    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="y")
+    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="y", bf16_out=True)
 
 
 def test_fwd_inference_full_size_sampled():
@@ -180,7 +180,7 @@ def test_fwd_inference_full_size_sampled():
     ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, rows=rows)
     tau = preact_tau(inp.x[rows], inp.W_up, ref["pre"])
     compare_hidden(h_gpu[rows], ref["h"], h_gpu[rows] != 0, ref["active"] != 0, ref["pre"], tau)
-    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], ref["y"], what="y rows")
+    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], ref["y"], what="y rows", bf16_out=True)
     dens = got.nnz.sum() / (M * F)
     assert 0.007 < dens < 0.013  # ~99 % sparse
 
@@ -207,8 +207,8 @@ def test_fwd_gated_decode(name):
     diff = act_gpu != (ref["active"] != 0)
     assert not (diff & (np.abs(ref["pre"]) > tau)).any()
     both = act_gpu & (ref["active"] != 0)
-    assert_close_rms(bf16_f64(h_gpu)[both], bf16_f64(ref["h"])[both], what="gated h")
-    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="y")
+    assert_close_rms(bf16_f64(h_gpu)[both], bf16_f64(ref["h"])[both], what="gated h", bf16_out=True)
+    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="y", bf16_out=True)
 
 
 def test_fwd_capacity_overflow():
@@ -262,7 +262,7 @@ def test_bwd_matches_oracle(M, d, F, T, bias, l1, seed):
     X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, fw["h"], inp.dy))
     _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1)
     gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1)
-    assert_close_rms(dx, dx_ref, what="dx")
+    assert_close_rms(dx, dx_ref, what="dx", bf16_out=True)
     assert_close_rms(dWu, gu, what="dW_up")
     assert_close_rms(dWd, gd, what="dW_down")
     assert_close_rms(db, gb, what="db")
@@ -282,7 +282,7 @@ def test_bwd_inference_size_sampled():
     cols = np.r_[0, F - 1, rng.integers(0, F, 14)].astype(np.int32)
     _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1, rows=rows)
     gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1, cols=cols)
-    assert_close_rms(dx[rows], dx_ref, what="dx rows")
+    assert_close_rms(dx[rows], dx_ref, what="dx rows", bf16_out=True)
     assert_close_rms(dWu[cols], gu, what="dW_up cols")
     assert_close_rms(dWd[cols], gd, what="dW_down cols")
     assert_close_rms(db[cols], gb, what="db cols")
@@ -313,4 +313,4 @@ def test_dense_baseline_matches_oracle(M, d, F):
     hg = host_bf16_bits(h)
     tau = preact_tau(inp.x, inp.W_up, ref["pre"])
     compare_hidden(hg, ref["h"], hg != 0, ref["active"] != 0, ref["pre"], tau)
-    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="dense y")
+    assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="dense y", bf16_out=True)
