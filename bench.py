@@ -298,7 +298,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # ---- end to end through the public API with host buffers
     e2e = None
-    if rank == 0 or True:
+    if not args.no_extras:
         xh = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).pin_memory()
         dyh = torch.from_numpy(np.ascontiguousarray(inp.dy).view(np.int16)).pin_memory()
         yh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
@@ -328,7 +328,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     WdT = L.Wd.view(inp.F, inp.d).t().contiguous()
     hd = torch.empty(inp.M, inp.F, dtype=torch.int16, device="cuda")
     dts = []
-    for i in range(13):
+    for i in range(0 if args.no_extras else 13):
         flush.fill_(i & 0xff)
         a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -336,10 +336,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         b2.record(stream)
         dts.append((a, b2))
     torch.cuda.synchronize()
-    dense_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in dts[3:])
+    dense_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in dts[3:]) if dts else None
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.no_extras:
         rate, S, dt, cores = oracle_rate(inp, args.cpu_budget)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"first {S} of {inp.M} tokens, same weights, fwd + bwd, {dt:.1f} s"}
@@ -375,6 +375,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the e2e, dense and CPU legs (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
