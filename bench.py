@@ -121,13 +121,14 @@ def oracle_step(inp: syn.FFNInputs, S: int):
 
 
 def oracle_rate(inp: syn.FFNInputs, budget_s: float):
-    """Tokens/s of the oracle on a sample sized to take about budget_s."""
+    """Tokens/s of the oracle on a sample of the workload sized to take about budget_s."""
     import oracle
     oracle.build()
+    S0 = 32
     t0 = time.perf_counter()
-    oracle_step(inp, 2)
-    t2 = time.perf_counter() - t0
-    S = int(max(1, min(inp.M, 2 * budget_s / max(t2, 1e-3))))
+    oracle_step(inp, S0)
+    t_probe = time.perf_counter() - t0
+    S = int(max(1, min(inp.M, S0 * budget_s / max(t_probe, 1e-3))))
     t0 = time.perf_counter()
     oracle_step(inp, S)
     dt = time.perf_counter() - t0
@@ -142,11 +143,11 @@ def run_reference(args, rank: int, world: int):
     inp = syn.config_inputs(CONFIG_NAME, with_dy=True)
     total_budget = 150.0
     per_step = total_budget / max(1, args.steps + args.warmup)
-    # size the per-step sample from a 2-token probe
+    # size the per-step sample from a 32-token probe
     t0 = time.perf_counter()
-    oracle_step(inp, 2)
-    t2 = time.perf_counter() - t0
-    S = int(max(1, min(inp.M, 2 * per_step / max(t2, 1e-3))))
+    oracle_step(inp, 32)
+    t_probe = time.perf_counter() - t0
+    S = int(max(1, min(inp.M, 32 * per_step / max(t_probe, 1e-3))))
     for _ in range(args.warmup):
         oracle_step(inp, S)
     times = []
