@@ -23,8 +23,11 @@ OP_PACK, OP_SPMM_DOWN, OP_FFN_FWD, OP_FFN_BWD, OP_GATED_FWD = 0, 1, 2, 3, 4
 EXPORTED_SYMBOLS = (
     "twell_status_string", "twell_buf_slots_bound", "twell_workspace_bytes", "twell_device_sm_count",
     "twell_pack", "twell_up_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd",
-    "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check",
+    "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
 )
+
+# Size of the library-owned workspace behind twell_ffn_fwd_static_ws.
+STATIC_WS_BYTES = 32 * 1024 * 1024
 
 
 class TwellError(RuntimeError):
@@ -75,6 +78,8 @@ def load_library(path: str | None = None):
     lib.twell_ffn_bwd.argtypes = [P, P, P, BUFP, P, I32, F32, P, P, P, P, P, SZ, P, P]
     lib.twell_dense_ffn_fwd.restype = I32
     lib.twell_dense_ffn_fwd.argtypes = [P, P, P, P, I32, I32, I32, P, P, P, P]
+    lib.twell_ffn_fwd_static_ws.restype = I32
+    lib.twell_ffn_fwd_static_ws.argtypes = [P, P, P, P, P, I32, I32, I32, I32, BUFP, P, P, P]
     lib.twell_check.restype = I32
     lib.twell_check.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     _lib = lib
@@ -189,6 +194,18 @@ def twell_ffn_fwd(x, W_up, W_gate, b, W_down, T: int, h_out: TwellBuffers, y, ws
         _ptr(W_down, "W_down", bytes_per_elem=2, numel=F * d), M, d, F, T, h_out.ref,
         _ptr(y, "y", bytes_per_elem=2, numel=M * d), _ptr(ws, "ws"), ws.numel() * ws.element_size(),
         _ptr(status, "status", bytes_per_elem=4), _stream(stream)), "twell_ffn_fwd")
+
+
+def twell_ffn_fwd_static_ws(x, W_up, W_gate, b, W_down, T: int, h_out: TwellBuffers, y, status, stream=None):
+    """twell_ffn_fwd on the library-owned static workspace (no allocation)."""
+    M, d = x.shape
+    F = W_up.shape[0]
+    _check(load_library().twell_ffn_fwd_static_ws(
+        _ptr(x, "x", bytes_per_elem=2), _ptr(W_up, "W_up", bytes_per_elem=2, numel=F * d),
+        _ptr(W_gate, "W_gate", bytes_per_elem=2, numel=F * d), _ptr(b, "b", bytes_per_elem=4, numel=F),
+        _ptr(W_down, "W_down", bytes_per_elem=2, numel=F * d), M, d, F, T, h_out.ref,
+        _ptr(y, "y", bytes_per_elem=2, numel=M * d), _ptr(status, "status", bytes_per_elem=4),
+        _stream(stream)), "twell_ffn_fwd_static_ws")
 
 
 def twell_ffn_bwd(x, W_up, W_down, h: TwellBuffers, dy, l1: float, dx, dW_up, dW_down, db, ws, status,

@@ -181,6 +181,35 @@ twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const 
                                  const uint16_t* W_downT, int M, int d, int F,
                                  uint16_t* h_dense, uint16_t* y, int32_t* status, void* stream);
 
+/*
+ * twell_ffn_fwd_static_ws — twell_ffn_fwd for callers that cannot allocate
+ * device memory. The paper has no counterpart; this is a convenience of this
+ * library. It is meant for code that has no allocator to call (a plugin inside
+ * a host framework that owns all device memory) or must not call one (a
+ * latency-critical decode loop, where cudaMalloc/cudaFree synchronise the
+ * device). Same arguments and results as twell_ffn_fwd, without ws/ws_bytes:
+ * the workspace is a library-owned device array of TWELL_STATIC_WS_BYTES that
+ * every GPU which loads the library keeps until the process exits.
+ *   - Returns TWELL_ERR_WORKSPACE, with nothing enqueued, when the problem
+ *     needs more workspace than the array holds
+ *     (twell_workspace_bytes(TWELL_OP_FFN_FWD or TWELL_OP_GATED_FWD, M, d, F,
+ *     T, h_out->cap_slots) > TWELL_STATIC_WS_BYTES); decode shapes such as
+ *     M <= 64, d_model = 4096, d_ff = 14336 fit.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents: calls whose work overlaps on the GPU (different streams, or
+ *     different host threads, without ordering between them) race on it and
+ *     corrupt each other's results. Serialise them, e.g. on one stream.
+ *   - The allocation-free guarantee covers this call only; the caller still
+ *     owns x, the weights, b, y, h_out's arrays and status.
+ */
+#define TWELL_STATIC_WS_BYTES (32u * 1024u * 1024u)
+twell_status twell_ffn_fwd_static_ws(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate,
+                                     const float* b, const uint16_t* W_down, int M, int d, int F, int T,
+                                     const twell_buf* h_out, uint16_t* y, int32_t* status, void* stream);
+
 /* Number of kernels this library has launched in this process (host-side
  * counter, all devices). Lets a caller count the library's launches in a
  * timed region. */
