@@ -123,8 +123,7 @@ twell_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TWELL_OK : T
 bool dims_ok(int M, int d, int F) { return M > 0 && d > 0 && F > 0 && d % 8 == 0 && F % 8 == 0; }
 
 // Limits of this build's kernels.
-constexpr int kMaxD = 4096;      // row dot products keep 16 chunks of 256 columns per warp in registers
-constexpr int kMaxFBwd = 28672;  // per-block column masks of the backward live in shared memory
+constexpr int kMaxD = 4096;  // the gated up products keep 16 chunks of 256 columns per warp in registers
 
 }  // namespace
 
@@ -265,7 +264,7 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
         return TWELL_ERR_INVALID_ARG;
     twell_status st = check_buf(h, M, F, h->T);
     if (st != TWELL_OK) return st;
-    if (d > kMaxD || F > kMaxFBwd || h->cap_slots >= (int64_t)INT32_MAX) return TWELL_ERR_UNSUPPORTED;
+    if (h->cap_slots >= (int64_t)INT32_MAX) return TWELL_ERR_UNSUPPORTED;
     const size_t need = carve_bwd(nullptr, M, F, h->cap_slots, nullptr);
     if (!ws || ws_bytes < need) return TWELL_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;

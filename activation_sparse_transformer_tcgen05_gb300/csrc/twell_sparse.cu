@@ -70,6 +70,68 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w)
     acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
 }
 
+// acc[0..7] += v * (8 bf16 in w) with v a bf16 value (low 16 bits of vbits):
+// fma.rn.f32.bf16 multiplies two bf16 factors and accumulates in fp32. Their
+// product is exact in fp32, so this rounds exactly like fmaf on the widened
+// values, without the widening instructions.
+__device__ __forceinline__ void fma2_bf16(float& a0, float& a1, uint32_t w2, uint32_t vbits)
+{
+    asm("{\n"
+        ".reg .b16 lo, hi, vb;\n"
+        "mov.b32 {lo, hi}, %2;\n"
+        "cvt.u16.u32 vb, %3;\n"
+        "fma.rn.f32.bf16 %0, vb, lo, %0;\n"
+        "fma.rn.f32.bf16 %1, vb, hi, %1;\n"
+        "}\n"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w2), "r"(vbits));
+}
+
+__device__ __forceinline__ void fma8_bf16(float (&acc)[8], uint32_t vbits, const uint4& w)
+{
+    fma2_bf16(acc[0], acc[1], w.x, vbits);
+    fma2_bf16(acc[2], acc[3], w.y, vbits);
+    fma2_bf16(acc[4], acc[5], w.z, vbits);
+    fma2_bf16(acc[6], acc[7], w.w, vbits);
+}
+
+// sum_k a[k] * b[k] over 8 bf16 pairs in two independent fp32 chains.
+__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b)
+{
+    float s0 = 0.f, s1 = 0.f;
+    asm("{\n"
+        ".reg .b16 a0, a1, b0, b1;\n"
+        "mov.b32 {a0, a1}, %2;\n mov.b32 {b0, b1}, %6;\n"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n fma.rn.f32.bf16 %1, a1, b1, %1;\n"
+        "mov.b32 {a0, a1}, %3;\n mov.b32 {b0, b1}, %7;\n"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n fma.rn.f32.bf16 %1, a1, b1, %1;\n"
+        "mov.b32 {a0, a1}, %4;\n mov.b32 {b0, b1}, %8;\n"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n fma.rn.f32.bf16 %1, a1, b1, %1;\n"
+        "mov.b32 {a0, a1}, %5;\n mov.b32 {b0, b1}, %9;\n"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n fma.rn.f32.bf16 %1, a1, b1, %1;\n"
+        "}\n"
+        : "+f"(s0), "+f"(s1)
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+    return s0 + s1;
+}
+
+// After this, lane u holds the sum over all 32 lanes of v[u] (in v[0]): a
+// butterfly where each step keeps the half of the values that belongs to the
+// lane's side and adds the partner's copy of that half (31 shuffles in all).
+__device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+}
+
 // sum_k a[k] * b[k] over 8 bf16 pairs
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& b)
 {
@@ -303,29 +365,37 @@ __global__ void __launch_bounds__(kWarps * 32) k_spmm_rows(TwellView tw, const f
             const int m = min(32, ke - k0);
             int jl = 0;
             float vl = 0.f;
+            uint32_t vb = 0;
             if (lane < m) {
                 jl = tw.idx[base + k0 + lane];
-                vl = load_val(vals_f32, tw.val, base + k0 + lane);
+                if (vals_f32)
+                    vl = vals_f32[base + k0 + lane];
+                else
+                    vb = tw.val[base + k0 + lane];
             }
             int u = 0;
             for (; u + 4 <= m; u += 4) {
-                const int j0 = __shfl_sync(0xffffffffu, jl, u), j1 = __shfl_sync(0xffffffffu, jl, u + 1);
-                const int j2 = __shfl_sync(0xffffffffu, jl, u + 2), j3 = __shfl_sync(0xffffffffu, jl, u + 3);
-                const float v0 = __shfl_sync(0xffffffffu, vl, u), v1 = __shfl_sync(0xffffffffu, vl, u + 1);
-                const float v2 = __shfl_sync(0xffffffffu, vl, u + 2), v3 = __shfl_sync(0xffffffffu, vl, u + 3);
-                if (col_ok) {
-                    const uint4 w0 = ldg16(Wc + (size_t)j0 * d), w1 = ldg16(Wc + (size_t)j1 * d);
-                    const uint4 w2 = ldg16(Wc + (size_t)j2 * d), w3 = ldg16(Wc + (size_t)j3 * d);
-                    fma8(acc, v0, w0);
-                    fma8(acc, v1, w1);
-                    fma8(acc, v2, w2);
-                    fma8(acc, v3, w3);
+                uint4 w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int jj = __shfl_sync(0xffffffffu, jl, u + q);
+                    w[q] = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (vals_f32)
+                        fma8(acc, __shfl_sync(0xffffffffu, vl, u + q), w[q]);
+                    else
+                        fma8_bf16(acc, __shfl_sync(0xffffffffu, vb, u + q), w[q]);
                 }
             }
             for (; u < m; ++u) {
-                const int j0 = __shfl_sync(0xffffffffu, jl, u);
-                const float v0 = __shfl_sync(0xffffffffu, vl, u);
-                if (col_ok) fma8(acc, v0, ldg16(Wc + (size_t)j0 * d));
+                const int jj = __shfl_sync(0xffffffffu, jl, u);
+                const uint4 w = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
+                if (vals_f32)
+                    fma8(acc, __shfl_sync(0xffffffffu, vl, u), w);
+                else
+                    fma8_bf16(acc, __shfl_sync(0xffffffffu, vb, u), w);
             }
         }
     }
@@ -347,6 +417,56 @@ __global__ void __launch_bounds__(kWarps * 32) k_spmm_rows(TwellView tw, const f
         o.w = pack_bf16x2(acc[6], acc[7]);
         *reinterpret_cast<uint4*>(y + (size_t)r * d + c0) = o;
     }
+}
+
+// Backward SDDMM: dpre[slot] = dy[r] . W[idx] + l1 on the stored slots of
+// row r, 0 on its padding slots. A warp per row; the row's entries go in
+// batches of 32, lane u holding entry u's column. For each 256-column slice of
+// d every lane forms its 8-column share of the batch's dot products (16 rows of
+// W in flight at a time), then transpose_reduce32 leaves entry u's slice sum in
+// lane u, which adds the slices in order.
+__global__ void __launch_bounds__(kWarps * 32) k_sddmm_rows(TwellView tw, const uint16_t* __restrict__ dy,
+                                                            const uint16_t* __restrict__ W, int d, float l1,
+                                                            float* __restrict__ dpre, const int32_t* status)
+{
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
+    int Kt;
+    const int64_t base = row_base(tw, r, &Kt);
+    const int n = tw.nnz[r];
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        const int m = min(32, n - k0);
+        int jl = tw.idx[base + k0 + (lane < m ? lane : 0)];
+        float res = 0.f;
+        for (int c = 0; c < d; c += 256) {
+            const int col = c + lane * 8;
+            const bool col_ok = col < d;
+            const uint4 a = col_ok ? ldg16(dy + (size_t)r * d + col) : make_uint4(0, 0, 0, 0);
+            const uint16_t* Wc = W + (col_ok ? col : 0);
+            float v[32];
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                if (g * 16 < m) {
+                    uint4 w[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int jj = __shfl_sync(0xffffffffu, jl, g * 16 + q);
+                        w[q] = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[g * 16 + q] = dot8_bf16(a, w[q]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[g * 16 + q] = 0.f;
+                }
+            }
+            transpose_reduce32(v, lane);
+            res += v[0];
+        }
+        if (lane < m) dpre[base + k0 + lane] = res + l1;
+    }
+    for (int k = n + lane; k < Kt; k += 32) dpre[base + k] = 0.f;
 }
 
 // Row dot products on the stored entries: for entry (r, k) with column j,
@@ -434,13 +554,14 @@ __global__ void __launch_bounds__(kWarps * 32) k_row_dots(TwellView tw, const ui
 
 constexpr int kCscRows = 64;
 
-__global__ void __launch_bounds__(256) k_csc_mask(TwellView tw, unsigned long long* __restrict__ masks,
-                                                  const int32_t* status)
+__global__ void __launch_bounds__(256) k_csc_mask(TwellView tw, int col_range,
+                                                  unsigned long long* __restrict__ masks, const int32_t* status)
 {
-    extern __shared__ unsigned long long s_mask[];  // [F]
+    extern __shared__ unsigned long long s_mask[];  // [col_range]
     const int b = blockIdx.x;
+    const int jlo = blockIdx.y * col_range, jhi = min(tw.F, jlo + col_range);
     if (has_error(status)) return;
-    for (int j = threadIdx.x; j < tw.F; j += blockDim.x) s_mask[j] = 0ull;
+    for (int j = threadIdx.x; j < jhi - jlo; j += blockDim.x) s_mask[j] = 0ull;
     __syncthreads();
     const int r0 = b * kCscRows, r1 = min(tw.M, r0 + kCscRows);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -449,10 +570,13 @@ __global__ void __launch_bounds__(256) k_csc_mask(TwellView tw, unsigned long lo
         const int64_t base = row_base(tw, r, &Kt);
         const int n = tw.nnz[r];
         const unsigned long long bit = 1ull << (r - r0);
-        for (int k = lane; k < n; k += 32) atomicOr(&s_mask[tw.idx[base + k]], bit);
+        for (int k = lane; k < n; k += 32) {
+            const int j = tw.idx[base + k];
+            if (j >= jlo && j < jhi) atomicOr(&s_mask[j - jlo], bit);
+        }
     }
     __syncthreads();
-    for (int j = threadIdx.x; j < tw.F; j += blockDim.x) masks[(size_t)b * tw.F + j] = s_mask[j];
+    for (int j = threadIdx.x; j < jhi - jlo; j += blockDim.x) masks[(size_t)b * tw.F + jlo + j] = s_mask[j];
 }
 
 // 32 columns per block: start[b][j] = sum over blocks b' < b of popc(mask[b'][j]);
@@ -491,31 +615,32 @@ __global__ void __launch_bounds__(1024) k_csc_colscan(const unsigned long long* 
     if (ty == 0 && j < F) colcnt[j] = s_carry[tx];
 }
 
-// Single block: ptr[0..n] = exclusive prefix of cnt[0..n).
+// Single block: ptr[0..n] = exclusive prefix of cnt[0..n). Each thread scans
+// a run of consecutive elements; the run totals are scanned across the block.
 __global__ void __launch_bounds__(1024) k_scan_i32(const int32_t* __restrict__ cnt, int n, int32_t* __restrict__ ptr,
                                                    const int32_t* status)
 {
     __shared__ int s_warp[32];
-    __shared__ int s_carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (has_error(status)) return;
-    if (tid == 0) s_carry = 0;
+    const int per = (n + 1023) / 1024;
+    const int i0 = tid * per;
+    int local = 0;
+    for (int k = 0; k < per; ++k)
+        if (i0 + k < n) local += cnt[i0 + k];
+    const int incl = warp_incl_scan(local, lane);
+    if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += 1024) {
-        const int i = i0 + tid;
-        const int v = i < n ? cnt[i] : 0;
-        int incl = warp_incl_scan(v, lane);
-        if (lane == 31) s_warp[warp] = incl;
-        __syncthreads();
-        if (warp == 0) s_warp[lane] = warp_incl_scan(s_warp[lane], lane);
-        __syncthreads();
-        incl += (warp > 0 ? s_warp[warp - 1] : 0);
-        if (i < n) ptr[i] = s_carry + incl - v;
-        __syncthreads();
-        if (tid == 0) s_carry += s_warp[31];
-        __syncthreads();
+    if (warp == 0) s_warp[lane] = warp_incl_scan(s_warp[lane], lane);
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? s_warp[warp - 1] : 0);
+    for (int k = 0; k < per; ++k) {
+        if (i0 + k < n) {
+            ptr[i0 + k] = run;
+            run += cnt[i0 + k];
+        }
     }
-    if (tid == 0) ptr[n] = s_carry;
+    if (tid == 1023) ptr[n] = run;
 }
 
 __global__ void k_csc_scatter(TwellView tw, const unsigned long long* __restrict__ masks,
@@ -566,34 +691,37 @@ __global__ void __launch_bounds__(kWarps * 32) k_wgrad(TwellView tw, const int32
     for (int b0 = e0; b0 < e1; b0 += 32) {
         const int m = min(32, e1 - b0);
         int rl = 0;
-        float hl = 0.f, pl = 0.f;
+        uint32_t hl = 0;
+        float pl = 0.f;
         if (lane < m) {
             rl = crow[b0 + lane];
             const int s = cslot[b0 + lane];
-            hl = bf16_to_f32(tw.val[s]);
+            hl = tw.val[s];
             pl = dpre[s];
         }
         bsum += pl;
         int u = 0;
-        for (; u + 2 <= m; u += 2) {
-            const int ra = __shfl_sync(0xffffffffu, rl, u), rb = __shfl_sync(0xffffffffu, rl, u + 1);
-            const float ha = __shfl_sync(0xffffffffu, hl, u), hb = __shfl_sync(0xffffffffu, hl, u + 1);
-            const float pa = __shfl_sync(0xffffffffu, pl, u), pb = __shfl_sync(0xffffffffu, pl, u + 1);
-            if (col_ok) {
-                const uint4 dya = ldg16(dy + (size_t)ra * d + c0), xa = ldg16(x + (size_t)ra * d + c0);
-                const uint4 dyb = ldg16(dy + (size_t)rb * d + c0), xb = ldg16(x + (size_t)rb * d + c0);
-                fma8(ad, ha, dya);
-                fma8(au, pa, xa);
-                fma8(ad, hb, dyb);
-                fma8(au, pb, xb);
+        for (; u + 4 <= m; u += 4) {
+            uint4 dv[4], xv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int rr = __shfl_sync(0xffffffffu, rl, u + q);
+                dv[q] = col_ok ? ldg16(dy + (size_t)rr * d + c0) : make_uint4(0, 0, 0, 0);
+                xv[q] = col_ok ? ldg16(x + (size_t)rr * d + c0) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                fma8_bf16(ad, __shfl_sync(0xffffffffu, hl, u + q), dv[q]);
+                fma8(au, __shfl_sync(0xffffffffu, pl, u + q), xv[q]);
             }
         }
-        if (u < m) {
-            const int ra = __shfl_sync(0xffffffffu, rl, u);
-            const float ha = __shfl_sync(0xffffffffu, hl, u), pa = __shfl_sync(0xffffffffu, pl, u);
+        for (; u < m; ++u) {
+            const int rr = __shfl_sync(0xffffffffu, rl, u);
+            const uint32_t hv = __shfl_sync(0xffffffffu, hl, u);
+            const float pv = __shfl_sync(0xffffffffu, pl, u);
             if (col_ok) {
-                fma8(ad, ha, ldg16(dy + (size_t)ra * d + c0));
-                fma8(au, pa, ldg16(x + (size_t)ra * d + c0));
+                fma8_bf16(ad, hv, ldg16(dy + (size_t)rr * d + c0));
+                fma8(au, pv, ldg16(x + (size_t)rr * d + c0));
             }
         }
     }
@@ -706,7 +834,9 @@ static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const
 cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float l1, float* dpre,
                          int32_t* status, cudaStream_t s)
 {
-    return launch_row_dots<0>(tw, dy, W, d, l1, dpre, nullptr, status, s);
+    count_launches(1);
+    k_sddmm_rows<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, dy, W, d, l1, dpre, status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16_t* W_up, int d, const float* gval,
@@ -724,11 +854,19 @@ void csc_plan(int M, int F, int* row_blocks, int* rows_per_block)
 
 cudaError_t launch_csc(const TwellView& tw, const CscWork& w, int32_t* status, cudaStream_t s)
 {
-    const size_t smem = (size_t)tw.F * sizeof(unsigned long long);
+    // split the columns so that the mask pass has at least two blocks per SM
+    int splits = (2 * 152 + w.row_blocks - 1) / w.row_blocks;
+    splits = splits < 1 ? 1 : splits;
+    int col_range = (tw.F + splits - 1) / splits;
+    col_range = (col_range + 31) / 32 * 32;
+    if (col_range < 256) col_range = 256;
+    if (col_range > 16384) col_range = 16384;  // shared-memory masks: 128 KB at most
+    const int ny = (tw.F + col_range - 1) / col_range;
+    const size_t smem = (size_t)col_range * sizeof(unsigned long long);
     cudaError_t e = cudaFuncSetAttribute(k_csc_mask, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     count_launches(4);
-    k_csc_mask<<<w.row_blocks, 256, smem, s>>>(tw, w.masks, status);
+    k_csc_mask<<<dim3(w.row_blocks, ny), 256, smem, s>>>(tw, col_range, w.masks, status);
     k_csc_colscan<<<(tw.F + 31) / 32, 1024, 0, s>>>(w.masks, w.row_blocks, tw.F, w.start, w.colcnt, status);
     k_scan_i32<<<1, 1024, 0, s>>>(w.colcnt, tw.F, w.colptr, status);
     k_csc_scatter<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, w.masks, w.start, w.colptr, w.crow, w.cslot,
