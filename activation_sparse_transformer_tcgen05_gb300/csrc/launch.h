@@ -37,6 +37,13 @@ cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_
 cudaError_t launch_fill_staged_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
                                     const TwellView& tw, float* gval, int32_t* status, cudaStream_t s);
 
+// One-block layout + fill for small problems (M <= 1024, M * NB <= 8192).
+bool small_fill_ok(int M, int NB);
+cudaError_t launch_layout_fill_small_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
+                                          const TwellView& tw, float* gval, int32_t* status, cudaStream_t s);
+cudaError_t launch_layout_fill_small_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
+                                          const TwellView& tw, int32_t* status, cudaStream_t s);
+
 // ---- Sparse products (twell_sparse.cu)
 // y[r,:] = sum_k v[r,k] * W[idx[r,k], :]; v is the TwELL's bf16 val (vals_f32 == nullptr)
 // or an fp32 array indexed by slot.

@@ -224,17 +224,26 @@ twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16
         ga.stage = w.stage;
         ga.NB = (F + kReluBN - 1) / kReluBN;
         if (e == cudaSuccess) e = launch_gemm(GEMM_TWELL_RELU, x, W_up, ga, sms, s);
-        if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
-        if (e == cudaSuccess) e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, status, s);
+        if (small_fill_ok(M, ga.NB)) {
+            if (e == cudaSuccess) e = launch_layout_fill_small_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, status, s);
+        } else {
+            if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
+            if (e == cudaSuccess) e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, status, s);
+        }
     } else {
         ga.rowsA = F;
         ga.rowsB = M;
         ga.gstage = w.gstage;
         ga.NB = (F + kGateBM - 1) / kGateBM;
         if (e == cudaSuccess) e = launch_gemm(GEMM_GATE_SWAP, W_gate, x, ga, sms, s);
-        if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
-        if (e == cudaSuccess)
-            e = launch_fill_staged_gate(w.gstage, w.stage_cnt, ga.NB, kGateBM, tw, w.gval, status, s);
+        if (small_fill_ok(M, ga.NB)) {
+            if (e == cudaSuccess)
+                e = launch_layout_fill_small_gate(w.gstage, w.stage_cnt, ga.NB, kGateBM, tw, w.gval, status, s);
+        } else {
+            if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
+            if (e == cudaSuccess)
+                e = launch_fill_staged_gate(w.gstage, w.stage_cnt, ga.NB, kGateBM, tw, w.gval, status, s);
+        }
         if (e == cudaSuccess) e = launch_gated_up(tw, x, W_up, d, w.gval, status, s);
     }
     return cuda_status(e);

@@ -331,6 +331,125 @@ __global__ void k_fill_staged_gate(const uint2* __restrict__ stage, const int32_
     }
 }
 
+// Layout and fill in one block, for small problems (M * NB <= kSmallFillMax
+// staging blocks, M <= 1024): the per-(row, block) counts go to shared memory
+// with one coalesced load, rows' nnz and block prefixes, tile widths and offsets
+// are computed there, and every thread then copies the entries of its (row,
+// block) pairs and writes padding. This replaces k_tile_layout + the warp-per-row
+// fill, whose dependent global round trips dominate at decode sizes.
+constexpr int kSmallFillMax = 8192;
+
+template <typename Entry>
+__global__ void __launch_bounds__(1024) k_layout_fill_small(const Entry* __restrict__ stage,
+                                                            const int32_t* __restrict__ stage_cnt, int NB, int BW,
+                                                            TwellView tw, float* gval, int32_t* status)
+{
+    __shared__ int s_cnt[kSmallFillMax];  // per (row, block): count, then exclusive prefix within the row
+    __shared__ int s_nnz[1024];
+    __shared__ long long s_off[1025];
+    __shared__ int s_K[1024];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (has_error(status)) return;
+    const int M = tw.M, total = M * NB;
+    for (int i = tid; i < total; i += 1024) s_cnt[i] = stage_cnt[i];
+    __syncthreads();
+    // per-row exclusive prefix over blocks and nnz (a warp per row)
+    for (int r = warp; r < M; r += 32) {
+        int carry = 0;
+        for (int nb0 = 0; nb0 < NB; nb0 += 32) {
+            const int nb = nb0 + lane;
+            const int c = nb < NB ? s_cnt[r * NB + nb] : 0;
+            const int incl = warp_incl_scan(c, lane);
+            if (nb < NB) s_cnt[r * NB + nb] = carry + incl - c;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            s_nnz[r] = carry;
+            tw.nnz[r] = carry;
+        }
+    }
+    __syncthreads();
+    // tile widths and offsets (one thread; at most 1024 tiles of at most 1024 rows in total)
+    if (tid == 0) {
+        long long off = 0;
+        for (int t = 0; t < tw.n_tiles; ++t) {
+            const int r0 = t * tw.T, rows = min(tw.T, M - r0);
+            int mx = 0;
+            for (int i = 0; i < rows; ++i) mx = max(mx, s_nnz[r0 + i]);
+            s_K[t] = mx;
+            tw.K[t] = mx;
+            s_off[t] = off;
+            tw.off[t] = off;
+            off += (long long)rows * mx;
+        }
+        s_off[tw.n_tiles] = off;
+        tw.off[tw.n_tiles] = off;
+        if (off > tw.cap) set_error(status, TWELL_ERR_CAPACITY);
+    }
+    __syncthreads();
+    if (s_off[tw.n_tiles] > tw.cap) return;
+    // entries
+    for (int i = tid; i < total; i += 1024) {
+        const int r = i / NB, nb = i - r * NB;
+        const int t = r / tw.T;
+        const long long base = s_off[t] + (long long)(r - t * tw.T) * s_K[t] + s_cnt[i];
+        const int c = stage_cnt[i];
+        const Entry* src = stage + (size_t)i * BW;
+        for (int e = 0; e < c; ++e) {
+            const Entry w = src[e];
+            if constexpr (sizeof(Entry) == 8) {
+                tw.idx[base + e] = (int)w.x;
+                gval[base + e] = __uint_as_float(w.y);
+            } else {
+                tw.idx[base + e] = nb * BW + (int)(w & 0xffffu);
+                tw.val[base + e] = (uint16_t)(w >> 16);
+            }
+        }
+    }
+    // padding
+    for (int r = warp; r < M; r += 32) {
+        const int t = r / tw.T;
+        const long long base = s_off[t] + (long long)(r - t * tw.T) * s_K[t];
+        for (int k = s_nnz[r] + lane; k < s_K[t]; k += 32) {
+            tw.idx[base + k] = -1;
+            tw.val[base + k] = 0;
+            if constexpr (sizeof(Entry) == 8) gval[base + k] = 0.f;
+        }
+    }
+}
+
+// Gated up products, one warp per stored slot over a persistent grid:
+// val[slot] = bf16(relu(g) * (x[r] . W_up[j])), g = gval[slot]. Slots are
+// visited in tile order; a slot's row and position come from off[] / K[].
+__global__ void __launch_bounds__(kWarps * 32) k_gated_up_slots(TwellView tw, const uint16_t* __restrict__ x,
+                                                                const uint16_t* __restrict__ W_up, int d,
+                                                                const float* __restrict__ gval,
+                                                                const int32_t* status)
+{
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = (long long)gridDim.x * kWarps;
+    if (has_error(status) || over_capacity(tw)) return;
+    const long long S = tw.off[tw.n_tiles];
+    int t = 0;
+    for (long long s = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5); s < S; s += nwarps) {
+        while (tw.off[t + 1] <= s) ++t;  // slots only grow, so the tile index only advances
+        const int Kt = tw.K[t];
+        const long long rel = s - tw.off[t];
+        const int i = (int)(rel / Kt), k = (int)(rel - (long long)i * Kt);
+        const int r = t * tw.T + i;
+        if (k >= tw.nnz[r]) continue;  // padding
+        const int j = tw.idx[s];
+        float acc = 0.f;
+        for (int c = lane * 8; c < d; c += 256) {
+            const uint4 a = ldg16(x + (size_t)r * d + c);
+            const uint4 w = ldg16(W_up + (size_t)j * d + c);
+            acc += dot8(a, w);
+        }
+        acc = warp_sum_f(acc);
+        if (lane == 0) tw.val[s] = f32_to_bf16_bits(fmaxf(gval[s], 0.f) * acc);
+    }
+}
+
 // -------------------------------------------------------- sparse products --
 
 // y[r, cols] = sum_k v[r,k] W[idx[r,k], cols] for one (row, 256-column group)
@@ -842,7 +961,31 @@ cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t
 cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16_t* W_up, int d, const float* gval,
                             int32_t* status, cudaStream_t s)
 {
+    if (tw.M <= 256) {
+        // few rows: spread the slots over the whole GPU, a warp per slot
+        count_launches(1);
+        k_gated_up_slots<<<2 * 152, kWarps * 32, 0, s>>>(tw, x, W_up, d, gval, status);
+        return cudaGetLastError();
+    }
     return launch_row_dots<1>(tw, x, W_up, d, 0.f, nullptr, gval, status, s);
+}
+
+bool small_fill_ok(int M, int NB) { return M <= 1024 && (long long)M * NB <= kSmallFillMax; }
+
+cudaError_t launch_layout_fill_small_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
+                                          const TwellView& tw, float* gval, int32_t* status, cudaStream_t s)
+{
+    count_launches(1);
+    k_layout_fill_small<uint2><<<1, 1024, 0, s>>>(stage, stage_cnt, NB, BM, tw, gval, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_layout_fill_small_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
+                                          const TwellView& tw, int32_t* status, cudaStream_t s)
+{
+    count_launches(1);
+    k_layout_fill_small<uint32_t><<<1, 1024, 0, s>>>(stage, stage_cnt, NB, BN, tw, nullptr, status);
+    return cudaGetLastError();
 }
 
 void csc_plan(int M, int F, int* row_blocks, int* rows_per_block)

@@ -228,6 +228,47 @@ def stage_roofline(name, ms, inp, slots, nnz, peaks):
             "traffic": None, "algorithmic": f"{by / 1e6:.1f} MB compulsory"}
 
 
+def decode_leg(tw, peaks, flush, stream, reps: int = 30):
+    """Gated decode forward (M = 1, 8, 64 tokens, d_model 4096, d_ff 14336, ~99.5 % sparse):
+    time of one twell_ffn_fwd call with L2 flushed before it, and its HBM roofline
+    (algorithmic bytes: W_gate once, the union of active W_up and W_down rows once, x, y)."""
+    out = {}
+    for name in ("decode1", "decode8", "decode64"):
+        inp = syn.config_inputs(name)
+        M, d, F, T = inp.M, inp.d, inp.F, inp.T
+        x, Wu, Wg, Wd = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_gate), dev16(inp.W_down)
+        b = torch.from_numpy(inp.b).cuda()
+        cap = M * F
+        buf = tw.TwellBuffers(M, F, T, cap)
+        y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+        ws = torch.empty(tw.twell_workspace_bytes(tw.OP_GATED_FWD, M, d, F, T, cap), dtype=torch.uint8,
+                         device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        evs = []
+        for i in range(reps + 3):
+            flush.fill_(i & 0xff)
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            tw.twell_ffn_fwd(x, Wu, Wg, b, Wd, T, buf, y, ws, st)
+            b2.record(stream)
+            if i >= 3:
+                evs.append((a, b2))
+        torch.cuda.synchronize()
+        if tw.twell_check(st) != 0:
+            raise RuntimeError(f"{name}: device status {tw.twell_check(st)}")
+        us = statistics.median(a.elapsed_time(b2) for a, b2 in evs) * 1000.0
+        n = buf.slots()
+        idx = buf.idx[:n].cpu().numpy()
+        union = int(len(np.unique(idx[idx >= 0])))
+        byts = F * d * 2 + 2 * union * d * 2 + 2 * M * d * 2 + F * 4
+        gbs = byts / (us * 1e-6) / 1e9
+        out[name] = {"us": us, "tokens_per_s": M / (us * 1e-6), "active_units_union": union,
+                     "algorithmic_MB": byts / 1e6, "achieved_GBs": gbs, "hbm_frac": gbs / peaks["hbm"],
+                     "dense_gated_roofline_us": 3 * F * d * 2 / (peaks["hbm"] * 1e9) * 1e6}
+        del x, Wu, Wg, Wd, buf, ws
+    return out
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import activation_sparse_transformer_tcgen05_gb300 as tw
     from activation_sparse_transformer_tcgen05_gb300 import build as tbuild
@@ -339,6 +380,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     dense_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in dts[3:]) if dts else None
 
+    decode = None if args.no_extras else decode_leg(tw, peaks, flush, stream)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.no_extras:
         rate, S, dt, cores = oracle_rate(inp, args.cpu_budget)
@@ -363,6 +406,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "fwd": {"value": world * inp.M / (ms_fwd / 1000.0), "unit": UNIT, "ms": ms_fwd},
         "stages": stages,
         "dense_tcgen05_fwd_ms": dense_ms,
+        "decode": decode,
         "wall_s_timed": t_wall,
     }
     print(json.dumps(line), flush=True)
