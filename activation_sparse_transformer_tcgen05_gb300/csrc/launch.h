@@ -12,6 +12,21 @@ namespace twell {
 extern std::atomic<long long> g_kernel_launches;
 inline void count_launches(int n) { g_kernel_launches.fetch_add(n, std::memory_order_relaxed); }
 
+// Measurement hook (twell_set_kernel_timer): events recorded around one call site.
+struct KernelTimer {
+    int site;
+    cudaEvent_t begin, end;
+};
+extern KernelTimer g_timer;
+inline void timer_begin(int site, cudaStream_t s)
+{
+    if (g_timer.site == site && g_timer.begin) cudaEventRecord(g_timer.begin, s);
+}
+inline void timer_end(int site, cudaStream_t s)
+{
+    if (g_timer.site == site && g_timer.end) cudaEventRecord(g_timer.end, s);
+}
+
 // Device view of a TwELL (same fields as the public twell_buf).
 struct TwellView {
     int M, F, T, n_tiles;

@@ -188,7 +188,11 @@ twell_status twell_spmm_down(const twell_buf* h, const uint16_t* W_down, int d, 
     twell_status st = check_buf(h, h->M, h->F, h->T);
     if (st != TWELL_OK) return st;
     const TwellView tw = view_of(h);
-    return cuda_status(launch_spmm_rows(tw, nullptr, W_down, d, y, status, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    timer_begin(TWELL_SITE_SPMM_DOWN, s);
+    const cudaError_t e = launch_spmm_rows(tw, nullptr, W_down, d, y, status, s);
+    timer_end(TWELL_SITE_SPMM_DOWN, s);
+    return cuda_status(e);
 }
 
 twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b, int M,
@@ -223,7 +227,9 @@ twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16
         ga.rowsB = F;
         ga.stage = w.stage;
         ga.NB = (F + kReluBN - 1) / kReluBN;
+        timer_begin(TWELL_SITE_UP_GEMM, s);
         if (e == cudaSuccess) e = launch_gemm(GEMM_TWELL_RELU, x, W_up, ga, sms, s);
+        timer_end(TWELL_SITE_UP_GEMM, s);
         if (small_fill_ok(M, ga.NB)) {
             if (e == cudaSuccess) e = launch_layout_fill_small_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, status, s);
         } else {
@@ -235,7 +241,9 @@ twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16
         ga.rowsB = M;
         ga.gstage = w.gstage;
         ga.NB = (F + kGateBM - 1) / kGateBM;
+        timer_begin(TWELL_SITE_UP_GEMM, s);
         if (e == cudaSuccess) e = launch_gemm(GEMM_GATE_SWAP, W_gate, x, ga, sms, s);
+        timer_end(TWELL_SITE_UP_GEMM, s);
         if (small_fill_ok(M, ga.NB)) {
             if (e == cudaSuccess)
                 e = launch_layout_fill_small_gate(w.gstage, w.stage_cnt, ga.NB, kGateBM, tw, w.gval, status, s);
@@ -257,7 +265,11 @@ twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16
     twell_status st = twell_up_pack(x, W_up, W_gate, b, M, d, F, T, h_out, ws, ws_bytes, status, stream);
     if (st != TWELL_OK) return st;
     const TwellView tw = view_of(h_out);
-    return cuda_status(launch_spmm_rows(tw, nullptr, W_down, d, y, status, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    timer_begin(TWELL_SITE_SPMM_DOWN, s);
+    const cudaError_t e = launch_spmm_rows(tw, nullptr, W_down, d, y, status, s);
+    timer_end(TWELL_SITE_SPMM_DOWN, s);
+    return cuda_status(e);
 }
 
 twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down, const twell_buf* h,
@@ -282,10 +294,18 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
     const TwellView tw = view_of(h);
     BwdWs w;
     carve_bwd(ws, M, F, h->cap_slots, &w);
+    timer_begin(TWELL_SITE_SDDMM, s);
     cudaError_t e = launch_sddmm(tw, dy, W_down, d, l1_coef, w.dpre, status, s);
+    timer_end(TWELL_SITE_SDDMM, s);
+    timer_begin(TWELL_SITE_DX, s);
     if (e == cudaSuccess) e = launch_spmm_rows(tw, w.dpre, W_up, d, dx, status, s);
+    timer_end(TWELL_SITE_DX, s);
+    timer_begin(TWELL_SITE_CSC, s);
     if (e == cudaSuccess) e = launch_csc(tw, w.csc, status, s);
+    timer_end(TWELL_SITE_CSC, s);
+    timer_begin(TWELL_SITE_WGRAD, s);
     if (e == cudaSuccess) e = launch_wgrad(tw, w.csc, w.dpre, x, dy, d, dW_up, dW_down, db, status, s);
+    timer_end(TWELL_SITE_WGRAD, s);
     return cuda_status(e);
 }
 
@@ -319,6 +339,15 @@ twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const 
     g2.status = status;
     if (e == cudaSuccess) e = launch_gemm(GEMM_DENSE, h_dense, W_downT, g2, sms, s);
     return cuda_status(e);
+}
+
+twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end)
+{
+    if (site < TWELL_SITE_NONE || site > TWELL_SITE_WGRAD) return TWELL_ERR_INVALID_ARG;
+    g_timer.site = (ev_begin && ev_end) ? site : TWELL_SITE_NONE;
+    g_timer.begin = static_cast<cudaEvent_t>(ev_begin);
+    g_timer.end = static_cast<cudaEvent_t>(ev_end);
+    return TWELL_OK;
 }
 
 int64_t twell_kernel_launches(void) { return (int64_t)g_kernel_launches.load(std::memory_order_relaxed); }

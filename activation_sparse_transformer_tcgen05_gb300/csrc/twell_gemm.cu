@@ -408,7 +408,7 @@ cudaError_t launch_gemm(int mode, const uint16_t* A, const uint16_t* B, const Ge
                 const uint16_t* Bc = B + (size_t)t0 * a.K;
                 cudaError_t e;
                 if (bn == 16)
-                    e = run<16, GEMM_GATE_SWAP, 8>(A, Bc, c, t0, sm_count, s);
+                    e = run<16, GEMM_GATE_SWAP, 11>(A, Bc, c, t0, sm_count, s);
                 else if (bn == 32)
                     e = run<32, GEMM_GATE_SWAP, 8>(A, Bc, c, t0, sm_count, s);
                 else

@@ -14,6 +14,7 @@
 namespace twell {
 
 std::atomic<long long> g_kernel_launches{0};
+KernelTimer g_timer{0, nullptr, nullptr};
 
 namespace {
 
@@ -331,7 +332,7 @@ __global__ void k_fill_staged_gate(const uint2* __restrict__ stage, const int32_
     }
 }
 
-// Layout and fill in one block, for small problems (M * NB <= kSmallFillMax
+// Layout and fill without a separate layout pass, for small problems (M * NB <= kSmallFillMax
 // staging blocks, M <= 1024): the per-(row, block) counts go to shared memory
 // with one coalesced load, rows' nnz and block prefixes, tile widths and offsets
 // are computed there, and every thread then copies the entries of its (row,
@@ -365,11 +366,12 @@ __global__ void __launch_bounds__(1024) k_layout_fill_small(const Entry* __restr
         }
         if (lane == 0) {
             s_nnz[r] = carry;
-            tw.nnz[r] = carry;
+            if (blockIdx.x == 0) tw.nnz[r] = carry;
         }
     }
     __syncthreads();
-    // tile widths and offsets (one thread; at most 1024 tiles of at most 1024 rows in total)
+    // tile widths and offsets (one thread; at most 1024 tiles of at most 1024 rows in total).
+    // Every block computes the same layout; block 0 writes it out.
     if (tid == 0) {
         long long off = 0;
         for (int t = 0; t < tw.n_tiles; ++t) {
@@ -377,19 +379,23 @@ __global__ void __launch_bounds__(1024) k_layout_fill_small(const Entry* __restr
             int mx = 0;
             for (int i = 0; i < rows; ++i) mx = max(mx, s_nnz[r0 + i]);
             s_K[t] = mx;
-            tw.K[t] = mx;
             s_off[t] = off;
-            tw.off[t] = off;
+            if (blockIdx.x == 0) {
+                tw.K[t] = mx;
+                tw.off[t] = off;
+            }
             off += (long long)rows * mx;
         }
         s_off[tw.n_tiles] = off;
-        tw.off[tw.n_tiles] = off;
-        if (off > tw.cap) set_error(status, TWELL_ERR_CAPACITY);
+        if (blockIdx.x == 0) {
+            tw.off[tw.n_tiles] = off;
+            if (off > tw.cap) set_error(status, TWELL_ERR_CAPACITY);
+        }
     }
     __syncthreads();
     if (s_off[tw.n_tiles] > tw.cap) return;
-    // entries
-    for (int i = tid; i < total; i += 1024) {
+    // entries: (row, block) pairs spread over the blocks
+    for (int i = blockIdx.x * 1024 + tid; i < total; i += gridDim.x * 1024) {
         const int r = i / NB, nb = i - r * NB;
         const int t = r / tw.T;
         const long long base = s_off[t] + (long long)(r - t * tw.T) * s_K[t] + s_cnt[i];
@@ -406,8 +412,8 @@ __global__ void __launch_bounds__(1024) k_layout_fill_small(const Entry* __restr
             }
         }
     }
-    // padding
-    for (int r = warp; r < M; r += 32) {
+    // padding: rows spread over the blocks' warps
+    for (int r = blockIdx.x * 32 + warp; r < M; r += gridDim.x * 32) {
         const int t = r / tw.T;
         const long long base = s_off[t] + (long long)(r - t * tw.T) * s_K[t];
         for (int k = s_nnz[r] + lane; k < s_K[t]; k += 32) {
@@ -439,11 +445,21 @@ __global__ void __launch_bounds__(kWarps * 32) k_gated_up_slots(TwellView tw, co
         const int r = t * tw.T + i;
         if (k >= tw.nnz[r]) continue;  // padding
         const int j = tw.idx[s];
+        const uint16_t* xr = x + (size_t)r * d + lane * 8;
+        const uint16_t* wr = W_up + (size_t)j * d + lane * 8;
         float acc = 0.f;
-        for (int c = lane * 8; c < d; c += 256) {
-            const uint4 a = ldg16(x + (size_t)r * d + c);
-            const uint4 w = ldg16(W_up + (size_t)j * d + c);
-            acc += dot8(a, w);
+        // 8 chunks of 256 columns in flight at a time
+        for (int c0 = 0; c0 < d; c0 += 8 * 256) {
+            uint4 a[8], w[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int c = c0 + q * 256;
+                const bool ok = c + lane * 8 < d;
+                a[q] = ok ? ldg16(xr + c) : make_uint4(0, 0, 0, 0);
+                w[q] = ok ? ldg16(wr + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc += dot8_bf16(a[q], w[q]);
         }
         acc = warp_sum_f(acc);
         if (lane == 0) tw.val[s] = f32_to_bf16_bits(fmaxf(gval[s], 0.f) * acc);
@@ -456,14 +472,15 @@ __global__ void __launch_bounds__(kWarps * 32) k_gated_up_slots(TwellView tw, co
 // task. SPLIT warps share a task, each taking a contiguous share of the row's
 // entries; their partial sums are added in warp order through shared memory.
 template <int SPLIT>
-__global__ void __launch_bounds__(kWarps * 32) k_spmm_rows(TwellView tw, const float* __restrict__ vals_f32,
-                                                           const uint16_t* __restrict__ W, int d,
-                                                           uint16_t* __restrict__ y, const int32_t* status)
+__global__ void __launch_bounds__((SPLIT > kWarps ? SPLIT : kWarps) * 32) k_spmm_rows(
+    TwellView tw, const float* __restrict__ vals_f32, const uint16_t* __restrict__ W, int d,
+    uint16_t* __restrict__ y, const int32_t* status)
 {
-    __shared__ float red[SPLIT > 1 ? kWarps : 1][SPLIT > 1 ? 256 : 1];
+    constexpr int BW = SPLIT > kWarps ? SPLIT : kWarps;  // warps per block
+    __shared__ float red[SPLIT > 1 ? BW : 1][SPLIT > 1 ? 256 : 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ngroups = (d + 255) >> 8;
-    const int64_t task = (int64_t)blockIdx.x * (kWarps / SPLIT) + warp / SPLIT;
+    const int64_t task = (int64_t)blockIdx.x * (BW / SPLIT) + warp / SPLIT;
     const int sub = warp % SPLIT;
     if (has_error(status) || over_capacity(tw)) return;  // uniform across the block
     const int r = (int)(task / ngroups), g = (int)(task % ngroups);
@@ -909,7 +926,7 @@ cudaError_t launch_spmm_rows(const TwellView& tw, const float* vals_f32, const u
     if (tw.M >= 256) {
         k_spmm_rows<1><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
     } else {
-        k_spmm_rows<8><<<(unsigned)tasks, kWarps * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
+        k_spmm_rows<16><<<(unsigned)tasks, 16 * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
     }
     return cudaGetLastError();
 }
@@ -976,7 +993,8 @@ cudaError_t launch_layout_fill_small_gate(const uint2* stage, const int32_t* sta
                                           const TwellView& tw, float* gval, int32_t* status, cudaStream_t s)
 {
     count_launches(1);
-    k_layout_fill_small<uint2><<<1, 1024, 0, s>>>(stage, stage_cnt, NB, BM, tw, gval, status);
+    const int nblk = (tw.M * NB + 1023) / 1024;
+    k_layout_fill_small<uint2><<<nblk, 1024, 0, s>>>(stage, stage_cnt, NB, BM, tw, gval, status);
     return cudaGetLastError();
 }
 
@@ -984,7 +1002,8 @@ cudaError_t launch_layout_fill_small_relu(const uint32_t* stage, const int32_t* 
                                           const TwellView& tw, int32_t* status, cudaStream_t s)
 {
     count_launches(1);
-    k_layout_fill_small<uint32_t><<<1, 1024, 0, s>>>(stage, stage_cnt, NB, BN, tw, nullptr, status);
+    const int nblk = (tw.M * NB + 1023) / 1024;
+    k_layout_fill_small<uint32_t><<<nblk, 1024, 0, s>>>(stage, stage_cnt, NB, BN, tw, nullptr, status);
     return cudaGetLastError();
 }
 

@@ -24,7 +24,11 @@ EXPORTED_SYMBOLS = (
     "twell_status_string", "twell_buf_slots_bound", "twell_workspace_bytes", "twell_device_sm_count",
     "twell_pack", "twell_up_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd",
     "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
+    "twell_set_kernel_timer",
 )
+
+# Call sites of twell_set_kernel_timer.
+SITE_NONE, SITE_UP_GEMM, SITE_SPMM_DOWN, SITE_SDDMM, SITE_DX, SITE_CSC, SITE_WGRAD = range(7)
 
 # Size of the library-owned workspace behind twell_ffn_fwd_static_ws.
 STATIC_WS_BYTES = 32 * 1024 * 1024
@@ -70,6 +74,8 @@ def load_library(path: str | None = None):
     lib.twell_up_pack.restype = I32
     lib.twell_up_pack.argtypes = [P, P, P, P, I32, I32, I32, I32, BUFP, P, SZ, P, P]
     lib.twell_kernel_launches.restype = I64
+    lib.twell_set_kernel_timer.restype = I32
+    lib.twell_set_kernel_timer.argtypes = [I32, P, P]
     lib.twell_spmm_down.restype = I32
     lib.twell_spmm_down.argtypes = [BUFP, P, I32, P, P, P]
     lib.twell_ffn_fwd.restype = I32
@@ -165,6 +171,15 @@ def twell_pack(h: torch.Tensor, T: int, out: TwellBuffers, status: torch.Tensor,
 
 def twell_kernel_launches() -> int:
     return int(load_library().twell_kernel_launches())
+
+
+def twell_set_kernel_timer(site: int, ev_begin=None, ev_end=None):
+    """Record the torch.cuda.Events ev_begin / ev_end around the kernel at `site`
+    (SITE_*) on every launch until reset with site = SITE_NONE. The events must
+    have been recorded once before (torch creates them lazily)."""
+    b = ctypes.c_void_p(ev_begin.cuda_event) if ev_begin is not None else None
+    e = ctypes.c_void_p(ev_end.cuda_event) if ev_end is not None else None
+    _check(load_library().twell_set_kernel_timer(int(site), b, e), "twell_set_kernel_timer")
 
 
 def twell_up_pack(x, W_up, W_gate, b, T: int, h_out: TwellBuffers, ws, status, stream=None):

@@ -210,6 +210,23 @@ twell_status twell_ffn_fwd_static_ws(const uint16_t* x, const uint16_t* W_up, co
                                      const float* b, const uint16_t* W_down, int M, int d, int F, int T,
                                      const twell_buf* h_out, uint16_t* y, int32_t* status, void* stream);
 
+/*
+ * twell_set_kernel_timer — measurement hook. While set, every launch of the
+ * kernel at call site `site` is bracketed by cudaEventRecord(ev_begin) and
+ * cudaEventRecord(ev_end) on the launch's stream; ev_begin/ev_end are
+ * caller-created cudaEvent_t handles passed as void*. site = 0 (or NULL
+ * events) turns the hook off. Process-wide setting, not thread-safe: set it
+ * from the thread that launches. Sites:
+ *   1 up-projection GEMM (twell_up_pack / twell_ffn_fwd)
+ *   2 sparse down-projection (twell_spmm_down / twell_ffn_fwd)
+ *   3 backward SDDMM            4 backward dx
+ *   5 backward column lists (first to last of its kernels)
+ *   6 backward weight gradients
+ */
+enum { TWELL_SITE_NONE = 0, TWELL_SITE_UP_GEMM = 1, TWELL_SITE_SPMM_DOWN = 2, TWELL_SITE_SDDMM = 3,
+       TWELL_SITE_DX = 4, TWELL_SITE_CSC = 5, TWELL_SITE_WGRAD = 6 };
+twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end);
+
 /* Number of kernels this library has launched in this process (host-side
  * counter, all devices). Lets a caller count the library's launches in a
  * timed region. */
