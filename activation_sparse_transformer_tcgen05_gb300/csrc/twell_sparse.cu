@@ -556,53 +556,62 @@ __global__ void __launch_bounds__((SPLIT > kWarps ? SPLIT : kWarps) * 32) k_spmm
 }
 
 // Backward SDDMM: dpre[slot] = dy[r] . W[idx] + l1 on the stored slots of
-// row r, 0 on its padding slots. A warp per row; the row's entries go in
-// batches of 32, lane u holding entry u's column. For each 256-column slice of
-// d every lane forms its 8-column share of the batch's dot products (16 rows of
-// W in flight at a time), then transpose_reduce32 leaves entry u's slice sum in
-// lane u, which adds the slices in order.
-__global__ void __launch_bounds__(kWarps * 32) k_sddmm_rows(TwellView tw, const uint16_t* __restrict__ dy,
-                                                            const uint16_t* __restrict__ W, int d, float l1,
-                                                            float* __restrict__ dpre, const int32_t* status)
+// row r, 0 on its padding slots. A block per row, a warp per 256-column slice
+// of d (G = ceil(d/256) warps). The row's entries go in batches of 32 (lane u
+// holding entry u's column); each warp forms its slice's share of the batch's
+// 32 dot products (16 rows of W in flight at a time, two fp32 chains per
+// product on bf16 factors) and transpose_reduce32 leaves entry u's slice sum in
+// lane u. Warp 0 adds the G slice sums in slice order through shared memory.
+constexpr int kSddmmMaxSlices = 16;  // d <= 4096
+
+__global__ void __launch_bounds__(kSddmmMaxSlices * 32) k_sddmm_rows(TwellView tw, const uint16_t* __restrict__ dy,
+                                                                     const uint16_t* __restrict__ W, int d, float l1,
+                                                                     float* __restrict__ dpre, const int32_t* status)
 {
-    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
+    __shared__ float s_part[kSddmmMaxSlices][32];
+    const int r = blockIdx.x;
+    const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = blockDim.x >> 5;
+    if (has_error(status) || over_capacity(tw)) return;  // uniform across the block
     int Kt;
     const int64_t base = row_base(tw, r, &Kt);
     const int n = tw.nnz[r];
+    const int col = g * 256 + lane * 8;
+    const bool col_ok = col < d;
+    const uint4 a = col_ok ? ldg16(dy + (size_t)r * d + col) : make_uint4(0, 0, 0, 0);
+    const uint16_t* Wc = W + (col_ok ? col : 0);
     for (int k0 = 0; k0 < n; k0 += 32) {
         const int m = min(32, n - k0);
-        int jl = tw.idx[base + k0 + (lane < m ? lane : 0)];
-        float res = 0.f;
-        for (int c = 0; c < d; c += 256) {
-            const int col = c + lane * 8;
-            const bool col_ok = col < d;
-            const uint4 a = col_ok ? ldg16(dy + (size_t)r * d + col) : make_uint4(0, 0, 0, 0);
-            const uint16_t* Wc = W + (col_ok ? col : 0);
-            float v[32];
+        const int jl = tw.idx[base + k0 + (lane < m ? lane : 0)];
+        float v[32];
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                if (g * 16 < m) {
-                    uint4 w[16];
+        for (int h = 0; h < 2; ++h) {
+            if (h * 16 < m) {
+                uint4 w[16];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int jj = __shfl_sync(0xffffffffu, jl, g * 16 + q);
-                        w[q] = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[g * 16 + q] = dot8_bf16(a, w[q]);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[g * 16 + q] = 0.f;
+                for (int q = 0; q < 16; ++q) {
+                    const int jj = __shfl_sync(0xffffffffu, jl, h * 16 + q);
+                    w[q] = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
                 }
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[h * 16 + q] = dot8_bf16(a, w[q]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[h * 16 + q] = 0.f;
             }
-            transpose_reduce32(v, lane);
-            res += v[0];
         }
-        if (lane < m) dpre[base + k0 + lane] = res + l1;
+        transpose_reduce32(v, lane);
+        s_part[g][lane] = v[0];
+        __syncthreads();
+        if (g == 0) {
+            float tot = 0.f;
+            for (int q = 0; q < G; ++q) tot += s_part[q][lane];
+            if (lane < m) dpre[base + k0 + lane] = tot + l1;
+        }
+        __syncthreads();
     }
-    for (int k = n + lane; k < Kt; k += 32) dpre[base + k] = 0.f;
+    if (g == 0)
+        for (int k = n + lane; k < Kt; k += 32) dpre[base + k] = 0.f;
 }
 
 // Row dot products on the stored entries: for entry (r, k) with column j,
@@ -970,8 +979,10 @@ static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const
 cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float l1, float* dpre,
                          int32_t* status, cudaStream_t s)
 {
+    const int G = (d + 255) / 256;
+    if (G > kSddmmMaxSlices) return cudaErrorInvalidValue;
     count_launches(1);
-    k_sddmm_rows<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, dy, W, d, l1, dpre, status);
+    k_sddmm_rows<<<tw.M, G * 32, 0, s>>>(tw, dy, W, d, l1, dpre, status);
     return cudaGetLastError();
 }
 

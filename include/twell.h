@@ -160,8 +160,8 @@ twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16
  *   db        = column sums of dpre             [F]    fp32
  *   x, dy [M, d] bf16; W_up, W_down [F, d] bf16; M and F are h->M and h->F.
  *   h: the forward's TwELL; ws: at least twell_workspace_bytes(TWELL_OP_FFN_BWD,
- *   M, d, F, T, h->cap_slots) bytes, 256-byte aligned. Limit of this build:
- *   h->cap_slots < 2^31 (else TWELL_ERR_UNSUPPORTED).
+ *   M, d, F, T, h->cap_slots) bytes, 256-byte aligned. Limits of this build:
+ *   d <= 4096, h->cap_slots < 2^31 (else TWELL_ERR_UNSUPPORTED).
  * The reduction order of every sum is fixed (no floating-point atomics).
  */
 twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down,
