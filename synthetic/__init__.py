@@ -70,6 +70,18 @@ def normal(seed: int, stream: int, count: int) -> np.ndarray:
     return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
 
 
+def normal_at(seed: int, stream: int, index: np.ndarray) -> np.ndarray:
+    """Elements `index` of the stream normal(seed, stream, .) without drawing the rest."""
+    i = np.asarray(index, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        base = _stream_base(seed, stream)
+        z1 = _mix(base + (np.uint64(2) * i + np.uint64(1)) * _GAMMA)
+        z2 = _mix(base + (np.uint64(2) * i + np.uint64(2)) * _GAMMA)
+    u1 = ((z1 >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
+    u2 = ((z2 >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
+    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+
+
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round float32 values to bfloat16 (nearest, ties to even); returns uint16 bits.
 
@@ -168,19 +180,25 @@ def sparse_hidden(M: int, F: int, density: float, *, seed: int = 0,
                   row_skew_sigma: float = 0.0) -> np.ndarray:
     """A random nonnegative hidden matrix h [M, F] (bf16 bits) with given density.
 
-    Entry (r, j) is active when a uniform draw is below ``density`` (scaled by
-    the row's skew factor when ``row_skew_sigma > 0``, clipped to 1); active
-    values are |N(0,1)| + 2**-8 so that none rounds to zero.
+    Entry (r, j) is active when uniform draw r*F + j is below ``density`` (scaled
+    by the row's skew factor when ``row_skew_sigma > 0``, clipped to 1); an
+    active value is |z| + 2**-8 with z normal draw r*F + j, so none rounds to
+    zero. Generated in row chunks; only active entries draw their normal.
     """
-    u = uniform(seed, STREAM_MASK, M * F).reshape(M, F)
-    p = np.full((M, 1), density)
+    h = np.zeros((M, F), dtype=np.uint16)
     if row_skew_sigma > 0.0:
-        s = np.exp(row_skew_sigma * normal(seed, STREAM_ROW_SCALE, M))
-        p = np.clip(density * s, 0.0, 1.0)[:, None]
-    mask = u <= p
-    vals = np.abs(normal(seed, STREAM_VALUES, M * F).reshape(M, F)) + 2.0 ** -8
-    h = np.where(mask, vals, 0.0).astype(np.float32)
-    return to_bf16_bits(h)
+        p_row = np.clip(density * np.exp(row_skew_sigma * normal(seed, STREAM_ROW_SCALE, M)), 0.0, 1.0)
+    else:
+        p_row = np.full(M, density)
+    rows_per_chunk = max(1, (1 << 22) // max(F, 1))
+    for r0 in range(0, M, rows_per_chunk):
+        r1 = min(M, r0 + rows_per_chunk)
+        u = uniform(seed, STREAM_MASK, (r1 - r0) * F, start=r0 * F).reshape(r1 - r0, F)
+        rr, jj = np.nonzero(u <= p_row[r0:r1, None])
+        flat = (rr + r0).astype(np.uint64) * np.uint64(F) + jj.astype(np.uint64)
+        vals = np.abs(normal_at(seed, STREAM_VALUES, flat)) + 2.0 ** -8
+        h[rr + r0, jj] = to_bf16_bits(vals.astype(np.float32))
+    return h
 
 
 # The synthetic configurations of the layer, by name. Sizes, biases and tile

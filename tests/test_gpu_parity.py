@@ -314,3 +314,75 @@ def test_dense_baseline_matches_oracle(M, d, F):
     tau = preact_tau(inp.x, inp.W_up, ref["pre"])
     compare_hidden(hg, ref["h"], hg != 0, ref["active"] != 0, ref["pre"], tau)
     assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="dense y", bf16_out=True)
+
+
+# ------------------------------------------- training and skewed workloads ---
+
+def test_fwd_training_full_size_sampled():
+    """The training workload's forward at full size (M=16384, d=4096, F=16384)."""
+    inp = syn.config_inputs("training")
+    M, d, F, T = inp.M, inp.d, inp.F, inp.T
+    buf, y, st = _fwd(inp)
+    _status_ok(st)
+    got = twell_to_host(buf)
+    rows = np.r_[0, 127, 128, M - 1, np.random.default_rng(2).integers(0, M, 12)].astype(np.int32)
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, rows=rows)
+    h_rows = np.zeros((len(rows), F), np.uint16)
+    for i, r in enumerate(rows):
+        t, ii = divmod(int(r), T)
+        base = got.off[t] + ii * got.K[t]
+        n = got.nnz[r]
+        h_rows[i, got.idx[base:base + n]] = got.val[base:base + n]
+        assert np.all(got.idx[base + n:base + got.K[t]] == -1)
+    tau = preact_tau(inp.x[rows], inp.W_up, ref["pre"])
+    compare_hidden(h_rows, ref["h"], h_rows != 0, ref["active"] != 0, ref["pre"], tau)
+    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], ref["y"], what="y rows", bf16_out=True)
+    assert got.K.tolist() == [int(got.nnz[t * T:(t + 1) * T].max()) for t in range(M // T)]
+    assert 0.007 < got.nnz.sum() / (M * F) < 0.013
+
+
+def test_bwd_training_full_size_sampled():
+    """The training workload's backward at full size on a synthetic 99 %-sparse h."""
+    M, d, F, T, l1 = 16384, 4096, 16384, 128, 1e-4
+    h = syn.sparse_hidden(M, F, 0.0099, seed=31)
+    inp = syn.ffn_inputs(M, d, F, T, -2.33, seed=31, with_dy=True)
+    ref_tw = oracle.twell_pack(h, T)
+    dx, dWu, dWd, db = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, l1)
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, h, inp.dy))
+    rng = np.random.default_rng(6)
+    rows = np.r_[0, M - 1, rng.integers(0, M, 10)].astype(np.int32)
+    cols = np.r_[0, F - 1, rng.integers(0, F, 10)].astype(np.int32)
+    _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1, rows=rows)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1, cols=cols)
+    assert_close_rms(dx[rows], dx_ref, what="dx rows", bf16_out=True)
+    assert_close_rms(dWu[cols], gu, what="dW_up cols")
+    assert_close_rms(dWd[cols], gd, what="dW_down cols")
+    assert_close_rms(db[cols], gb, what="db cols")
+
+
+@pytest.mark.parametrize("name", ["sweep90", "sweep99", "sweep999"])
+def test_fwd_skewed_rows(name):
+    """Sweep workloads (d_model 4096, d_ff 16384, lognormal row scales on x) on
+    1024 of their 8192 token rows: uneven rows stretch the tile widths."""
+    c = syn.CONFIGS[name]
+    M, d, F, T = 1024, c["d"], c["F"], c["T"]
+    inp = syn.ffn_inputs(M, d, F, T, c["bias"], seed=0, row_skew_sigma=c["skew"])
+    buf, y, st = _fwd(inp)
+    _status_ok(st)
+    got = twell_to_host(buf)
+    code, _ = oracle.twell_unpack(oracle.Twell(M, F, T, got.nnz, got.K, got.off, got.idx, got.val))
+    assert code == 0
+    order = np.argsort(got.nnz)
+    rows = np.r_[order[:2], order[-3:], np.random.default_rng(3).integers(0, M, 5)].astype(np.int32)
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, rows=rows)
+    h_rows = np.zeros((len(rows), F), np.uint16)
+    for i, r in enumerate(rows):
+        t, ii = divmod(int(r), T)
+        base = got.off[t] + ii * got.K[t]
+        n = got.nnz[r]
+        h_rows[i, got.idx[base:base + n]] = got.val[base:base + n]
+    tau = preact_tau(inp.x[rows], inp.W_up, ref["pre"])
+    compare_hidden(h_rows, ref["h"], h_rows != 0, ref["active"] != 0, ref["pre"], tau)
+    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], ref["y"], what="y rows", bf16_out=True)
+    # skew makes the widest row of a tile several times its mean
+    assert got.K.max() > 2 * got.nnz.mean()

@@ -323,6 +323,7 @@ def test_generator_is_counter_based_and_seeded():
     assert not np.array_equal(a, c)
     u = syn.uniform(0, 3, 2000)
     np.testing.assert_array_equal(syn.uniform(0, 3, 500, start=1500), u[1500:])
+    np.testing.assert_array_equal(syn.normal_at(0, syn.STREAM_X, np.array([999, 3, 0])), a[[999, 3, 0]])
     assert abs(a.mean()) < 0.15 and abs(a.std() - 1) < 0.1
     np.testing.assert_array_equal(syn.to_bf16_bits(a.astype(np.float32)),
                                   _torch_bf16_bits(a.astype(np.float32)))
