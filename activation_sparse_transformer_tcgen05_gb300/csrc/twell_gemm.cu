@@ -62,6 +62,78 @@ __device__ __forceinline__ void fail(int32_t* status, volatile int* abort_flag)
     *abort_flag = 1;
 }
 
+// TwELL epilogue of one accumulator row (one thread): bias, ReLU, bf16
+// rounding, and the row's nonzeros of this BN-column block appended to its
+// staging segment as (bf16 << 16 | column within the block), ascending.
+template <int BN>
+__device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int nb, const GemmArgs& a,
+                                              const float* bias_sm)
+{
+    const bool row_ok = row < a.rowsA;
+    uint32_t* st = a.stage + ((size_t)(row_ok ? row : 0) * a.NB + nb) * BN;
+    int cnt = 0;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32_wait(tbase + ch * 32, v);
+        // Straight-line per column (no branch): bias from 128-bit shared
+        // loads, the test, the rounding, and a predicated store, so that the
+        // 32 columns of a chunk overlap instead of each waiting on the last.
+        const float4* b4 = reinterpret_cast<const float4*>(bias_sm + ch * 32);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const float4 bb = b4[g];
+            const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = g * 4 + e;
+                const float p = __uint_as_float(v[c]) + bv[e];
+                const uint32_t hb = f32_to_bf16_bits(p);
+                const bool act = row_ok && p > 0.f && hb != 0u;
+                if (act) st[cnt] = (hb << 16) | (uint32_t)(ch * 32 + c);
+                cnt += act ? 1 : 0;
+            }
+        }
+    }
+    if (row_ok) {
+        a.stage_cnt[(size_t)row * a.NB + nb] = cnt;
+        if (cnt) atomicAdd(&a.nnz[row], cnt);
+    }
+}
+
+// Dense epilogue of one accumulator row: bias, optional ReLU, bf16 stores.
+template <int BN>
+__device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int nb, const GemmArgs& a,
+                                              const float* bias_sm)
+{
+    const bool row_ok = row < a.rowsA;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32_wait(tbase + ch * 32, v);
+        if (row_ok) {
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+                const int col = nb * BN + ch * 32 + g8 * 8;
+                if (col < a.rowsB) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        f[e] = __uint_as_float(v[g8 * 8 + e]) + bias_sm[ch * 32 + g8 * 8 + e];
+                        if (a.relu) f[e] = fmaxf(f[e], 0.f);
+                    }
+                    uint4 o;
+                    o.x = pack_bf16x2(f[0], f[1]);
+                    o.y = pack_bf16x2(f[2], f[3]);
+                    o.z = pack_bf16x2(f[4], f[5]);
+                    o.w = pack_bf16x2(f[6], f[7]);
+                    *reinterpret_cast<uint4*>(a.out + (size_t)row * a.ldo + col) = o;
+                }
+            }
+        }
+    }
+}
+
 template <int BN, int MODE, int STAGES>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs a, int tok0)
@@ -219,29 +291,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
 
             if constexpr (MODE == GEMM_TWELL_RELU) {
-                const int row = mb * BM + 32 * q + lane;
-                const bool row_ok = row < a.rowsA;
-                uint32_t* st = a.stage + ((size_t)(row_ok ? row : 0) * a.NB + nb) * BN;
-                int cnt = 0;
-#pragma unroll 1
-                for (int ch = 0; ch < BN / 32; ++ch) {
-                    uint32_t v[32];
-                    tmem_ld32_wait(tbase + ch * 32, v);
-                    if (row_ok) {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const float p = __uint_as_float(v[c]) + bias_sm[ch * 32 + c];
-                            if (p > 0.f) {
-                                const uint32_t hb = f32_to_bf16_bits(p);
-                                if (hb != 0u) st[cnt++] = (hb << 16) | (uint32_t)(ch * 32 + c);
-                            }
-                        }
-                    }
-                }
-                if (row_ok) {
-                    a.stage_cnt[(size_t)row * a.NB + nb] = cnt;
-                    if (cnt) atomicAdd(&a.nnz[row], cnt);
-                }
+                epi_twell_row<BN>(tbase, mb * BM + 32 * q + lane, nb, a, bias_sm);
             } else if constexpr (MODE == GEMM_GATE_SWAP) {
                 const int j = mb * BM + 32 * q + lane;  // hidden unit
                 const bool j_ok = j < a.rowsA;
@@ -288,33 +338,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             } else {  // GEMM_DENSE
-                const int row = mb * BM + 32 * q + lane;
-                const bool row_ok = row < a.rowsA;
-#pragma unroll 1
-                for (int ch = 0; ch < BN / 32; ++ch) {
-                    uint32_t v[32];
-                    tmem_ld32_wait(tbase + ch * 32, v);
-                    if (row_ok) {
-#pragma unroll
-                        for (int g8 = 0; g8 < 4; ++g8) {
-                            const int col = nb * BN + ch * 32 + g8 * 8;
-                            if (col < a.rowsB) {
-                                float f[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    f[e] = __uint_as_float(v[g8 * 8 + e]) + bias_sm[ch * 32 + g8 * 8 + e];
-                                    if (a.relu) f[e] = fmaxf(f[e], 0.f);
-                                }
-                                uint4 o;
-                                o.x = pack_bf16x2(f[0], f[1]);
-                                o.y = pack_bf16x2(f[2], f[3]);
-                                o.z = pack_bf16x2(f[4], f[5]);
-                                o.w = pack_bf16x2(f[6], f[7]);
-                                *reinterpret_cast<uint4*>(a.out + (size_t)row * a.ldo + col) = o;
-                            }
-                        }
-                    }
-                }
+                epi_dense_row<BN>(tbase, mb * BM + 32 * q + lane, nb, a, bias_sm);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -330,6 +354,237 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------- CTA pairs --
+//
+// The same GEMM on 256 x 256 tiles computed by a cluster of two CTAs with
+// tcgen05.mma.cta_group::2. Each CTA loads 128 rows of A and 128 of the
+// tile's 256 rows of B per k-block (32 KB instead of the 48 KB that a
+// 128 x 256 tile per CTA needs): the SM's share of operand traffic falls by a
+// third at the same MMA work per SM, which matters because the single-CTA
+// kernel is limited by how fast operands reach the SM.
+//
+//   warp 0 (both CTAs)   TMA producer of its own halves; completions are
+//                        counted on the even CTA's full barrier.
+//   warp 1 (both CTAs)   pair-collective TMEM allocation (all 512 columns:
+//                        two 256-column accumulators); in the even CTA lane 0
+//                        also issues the MMAs and commits to the barriers of
+//                        both CTAs (multicast).
+//   warps 2-5            epilogue of the CTA's own 128 rows x 256 columns;
+//                        each warp then arrives on the even CTA's tmem-empty
+//                        barrier (8 arrivals per accumulator).
+// Both CTAs always reach the pair-collective allocation, the deallocation and
+// the cluster barriers: the only early exit is taken by both, on a decision
+// read from the even CTA.
+
+constexpr int PAIR_M = 256;   // tile rows over the pair
+constexpr int PAIR_N = 256;   // tile columns (B rows over the pair)
+constexpr int HALF = 128;     // rows of A and of B held by one CTA
+
+template <int STAGES>
+struct PairLayout {
+    static constexpr int A_BYTES = HALF * BK * 2;
+    static constexpr int B_BYTES = HALF * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int BIAS_OFF = (MISC_OFF + 16 + 15) & ~15;
+    static constexpr int TOTAL = BIAS_OFF + PAIR_N * 4 + 1024;  // + alignment slack
+    static constexpr uint32_t TMEM_COLS = 2 * PAIR_N;
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
+};
+
+template <int MODE, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs a)
+{
+    static_assert(MODE == GEMM_TWELL_RELU || MODE == GEMM_DENSE, "row-wise epilogues only");
+    using L = PairLayout<STAGES>;
+    constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, PAIR_N);
+    constexpr int kEpiWarps = 2 * (kEpiThreads / 32);  // tmem-empty arrivals: both CTAs
+    extern __shared__ uint8_t smem_raw[];
+    // Same offset in both CTAs (same kernel, same static shared memory), as the
+    // pair MMA addresses the peer's operands with the leader's descriptors.
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* mma_done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* skip = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    volatile int* epi_fail = reinterpret_cast<volatile int*>(tmem_slot + 3);
+    float* bias_sm = reinterpret_cast<float*>(smem + L::BIAS_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        *skip = (leader && has_error(a.status)) ? 1 : 0;
+        *abort_flag = 0;
+        *epi_fail = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    cluster_sync();  // barriers of both CTAs initialised before either uses the other's
+    const int sk = ld_cluster_s32(cluster_addr(const_cast<int*>(skip), 0));
+    cluster_sync();  // the leader's flag has been read before anyone may leave
+    if (sk) return;  // an earlier kernel of this call failed; uniform over the pair
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_m = (a.rowsA + PAIR_M - 1) / PAIR_M;
+    const int num_n = (a.rowsB + PAIR_N - 1) / PAIR_N;
+    const int num_kb = (a.K + BK - 1) / BK;
+    const int num_tiles = num_m * num_n;
+    const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            const uint32_t full_leader = cluster_addr(full, 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+                const int mb = tile % num_m, nb = tile / num_m;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * L::STAGE_BYTES;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
+                    const uint32_t fb = full_leader + 8u * (uint32_t)stage;
+                    tma_load_2d_pair(sa, &tmA, kb * BK, mb * PAIR_M + (int)rank * HALF, fb);
+                    tma_load_2d_pair(sa + L::A_BYTES, &tmB, kb * BK, nb * PAIR_N + (int)rank * HALF, fb);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) fail(a.status, abort_flag);
+            // The last load issued into each stage must land before the CTA
+            // exits: the leader sees it on its full barrier, the peer on its
+            // empty barrier (the leader's MMAs consumed it).
+            for (int s = 0; s < STAGES; ++s) {
+                const long long n_s = issued / STAGES + (s < issued % STAGES ? 1 : 0);
+                if (n_s > 0) mbar_wait(leader ? &full[s] : &empty[s], (uint32_t)((n_s - 1) & 1), nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------- MMA issuer (even CTA) -----
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PAIR_N);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * L::STAGE_BYTES);
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + L::A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb | k) != 0);
+                    umma_commit_pair(&empty[stage], 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(&tfull[acc], 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) fail(a.status, abort_flag);
+            umma_commit_pair(mma_done, 0x1);  // every MMA issued above has finished once this arrives
+            mbar_wait(mma_done, 0, nullptr);
+        }
+    } else {
+        // --------------------------------------------------- epilogue -----
+        const int q = warp & 3;  // TMEM lane quarter this warp may read
+        const int et = threadIdx.x - 64;
+        const uint32_t tempty_leader = cluster_addr(tempty, 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+            const int mb = tile % num_m, nb = tile / num_m;
+            named_bar_sync(1, kEpiThreads);  // previous tile's shared-memory reads are done
+            for (int c = et; c < PAIR_N; c += kEpiThreads) {
+                const int col = nb * PAIR_N + c;
+                float bv;
+                if (MODE == GEMM_TWELL_RELU)
+                    bv = col < a.rowsB ? a.bias[col] : -INFINITY;
+                else
+                    bv = (a.bias && col < a.rowsB) ? a.bias[col] : 0.f;
+                bias_sm[c] = bv;
+            }
+            if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) *epi_fail = 1;
+            named_bar_sync(1, kEpiThreads);
+            if (*epi_fail) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * PAIR_N);
+            const int row = mb * PAIR_M + (int)rank * HALF + 32 * q + lane;
+            if constexpr (MODE == GEMM_TWELL_RELU)
+                epi_twell_row<PAIR_N>(tbase, row, nb, a, bias_sm);
+            else
+                epi_dense_row<PAIR_N>(tbase, row, nb, a, bias_sm);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (*epi_fail) fail(a.status, abort_flag);
+    }
+
+    // Neither CTA deallocates or exits while the pair's MMAs, loads or
+    // arrivals may still touch the other's tensor or shared memory.
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
     }
 }
 
@@ -383,6 +638,59 @@ cudaError_t run(const uint16_t* A, const uint16_t* B, const GemmArgs& a, int tok
     return cudaGetLastError();
 }
 
+// Clusters of two that can be resident at once for this kernel (0 = none).
+template <int MODE, int STAGES>
+int pair_capacity(cudaLaunchConfig_t cfg)
+{
+    static int cached[64] = {0};
+    static bool known[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!known[dev]) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<MODE, STAGES>, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        cached[dev] = n;
+        known[dev] = true;
+    }
+    return cached[dev];
+}
+
+// Launches the pair kernel; *launched = false (and nothing enqueued) when no
+// cluster of two fits, so the caller can take the single-CTA kernel.
+template <int MODE, int STAGES>
+cudaError_t run_pair(const uint16_t* A, const uint16_t* B, const GemmArgs& a, cudaStream_t s, bool* launched)
+{
+    using L = PairLayout<STAGES>;
+    *launched = false;
+    auto kern = k_gemm_pair<MODE, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = L::TOTAL;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int cap = pair_capacity<MODE, STAGES>(cfg);
+    if (cap <= 0) return cudaSuccess;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A, a.rowsA, a.K, HALF) || !make_map(&mb, B, a.rowsB, a.K, HALF)) return cudaErrorInvalidValue;
+    const int tiles = ((a.rowsA + PAIR_M - 1) / PAIR_M) * ((a.rowsB + PAIR_N - 1) / PAIR_N);
+    cfg.gridDim = dim3(2 * (tiles < cap ? tiles : cap), 1, 1);
+    count_launches(1);
+    *launched = true;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, a);
+}
+
 }  // namespace
 
 int gemm_block_n(int mode, int rowsB)
@@ -396,9 +704,19 @@ cudaError_t launch_gemm(int mode, const uint16_t* A, const uint16_t* B, const Ge
 {
     switch (mode) {
         case GEMM_TWELL_RELU:
-            return run<256, GEMM_TWELL_RELU, 4>(A, B, a, 0, sm_count, s);
-        case GEMM_DENSE:
-            return run<256, GEMM_DENSE, 4>(A, B, a, 0, sm_count, s);
+        case GEMM_DENSE: {
+            // Row-wise epilogues: 256 x 256 tiles on CTA pairs when there are
+            // more than 128 rows, else (or without room for a cluster of
+            // two) 128 x 256 tiles on single CTAs.
+            if (a.rowsA > HALF) {
+                bool launched = false;
+                const cudaError_t e = mode == GEMM_TWELL_RELU ? run_pair<GEMM_TWELL_RELU, 6>(A, B, a, s, &launched)
+                                                              : run_pair<GEMM_DENSE, 6>(A, B, a, s, &launched);
+                if (e != cudaSuccess || launched) return e;
+            }
+            return mode == GEMM_TWELL_RELU ? run<256, GEMM_TWELL_RELU, 4>(A, B, a, 0, sm_count, s)
+                                           : run<256, GEMM_DENSE, 4>(A, B, a, 0, sm_count, s);
+        }
         case GEMM_GATE_SWAP: {
             // B = x: token chunks of at most 64 rows, each a separate launch.
             const int bn = gemm_block_n(mode, a.rowsB);

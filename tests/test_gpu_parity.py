@@ -154,6 +154,7 @@ def test_fwd_integer_inputs_bit_exact():
     (64, 128, 512, 16, -2.33, 0),      # the tiny workload
     (200, 256, 1024, 128, -1.0, 1),    # several tiles, ragged last row tile
     (130, 136, 264, 7, -0.5, 2),       # ragged K (d % 64 != 0), F % 256 != 0, odd T
+    (712, 200, 800, 64, -1.2, 3),      # several 256 x 256 pair tiles each way, ragged in M, N and K
 ])
 def test_fwd_relu_matches_oracle(M, d, F, T, bias, seed):
     inp = syn.ffn_inputs(M, d, F, T, bias, seed=seed)
