@@ -90,6 +90,14 @@ cudaError_t launch_wgrad(const TwellView& tw, const CscWork& w, const float* dpr
 
 // ---- tcgen05 GEMM (twell_gemm.cu)
 enum GemmMode { GEMM_TWELL_RELU = 0, GEMM_GATE_SWAP = 1, GEMM_DENSE = 2 };
+// ---- gated decode tail (twell_sparse.cu): layout, fill, gated up and
+// down-projection in one cooperative launch; y == nullptr skips the
+// down-projection. `counter` must be 0 when it starts (grid barrier).
+bool decode_tail_ok(int M, int NB, int n_tiles);
+cudaError_t launch_decode_tail(const uint2* gstage, const int32_t* stage_cnt, int NB, int BM, const uint16_t* x,
+                               const uint16_t* W_up, const uint16_t* W_down, int d, const TwellView& tw,
+                               uint16_t* y, int32_t* counter, int32_t* status, cudaStream_t s);
+
 struct GemmArgs {
     int rowsA, rowsB, K;   // A [rowsA, K], B [rowsB, K], both bf16 K-major
     const float* bias;     // TWELL_RELU: per B row; GATE_SWAP: per A row; DENSE: per B row or null
@@ -97,7 +105,8 @@ struct GemmArgs {
     uint32_t* stage;       // TWELL_RELU staging [rowsA, NB, BN]
     uint2* gstage;         // GATE_SWAP staging [rowsB, NB, 128]
     int32_t* stage_cnt;    // [rows, NB]
-    int32_t* nnz;          // [rows], zeroed by the caller before the launch
+    int32_t* nnz;          // [rows], zeroed by the caller before the launch; null: not counted
+    int32_t* zero_word;    // if set, written 0 by the kernel (a counter the next kernel starts from)
     int NB;                // column blocks of the staging
     uint16_t* out;         // DENSE output [rowsA, ldo]
     int ldo;

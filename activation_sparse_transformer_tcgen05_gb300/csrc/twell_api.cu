@@ -50,6 +50,7 @@ struct FwdWs {
     uint32_t* stage;
     uint2* gstage;
     float* gval;
+    int32_t* counter;  // grid-barrier counter of the gated decode tail
 };
 
 size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out)
@@ -65,6 +66,7 @@ size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out)
         w.stage_cnt = c.take<int32_t>((size_t)M * NB);
         w.gstage = c.take<uint2>((size_t)M * NB * kGateBM);
         w.gval = c.take<float>((size_t)(cap > 0 ? cap : 1));
+        w.counter = c.take<int32_t>(1);
     }
     if (out) *out = w;
     return c.used;
@@ -195,10 +197,16 @@ twell_status twell_spmm_down(const twell_buf* h, const uint16_t* W_down, int d, 
     return cuda_status(e);
 }
 
-twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b, int M,
-                           int d, int F, int T, const twell_buf* h_out, void* ws, size_t ws_bytes, int32_t* status,
-                           void* stream)
+namespace {
+
+// The up-projection and TwELL packing. For gated decode batches the whole tail
+// after the gate GEMM runs as one launch, which then also computes
+// y = h W_down when W_down and y are given (*fused_down = true).
+twell_status up_pack_impl(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b, int M,
+                          int d, int F, int T, const twell_buf* h_out, void* ws, size_t ws_bytes, int32_t* status,
+                          void* stream, const uint16_t* W_down, uint16_t* y, bool* fused_down)
 {
+    *fused_down = false;
     if (!x || !W_up || !b || !status || !dims_ok(M, d, F)) return TWELL_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(W_up) || (W_gate && !aligned16(W_gate))) return TWELL_ERR_INVALID_ARG;
     twell_status st = check_buf(h_out, M, F, T);
@@ -215,7 +223,9 @@ twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16
     const TwellView tw = view_of(h_out);
     FwdWs w;
     carve_fwd(ws, gated, M, F, h_out->cap_slots, &w);
-    cudaError_t e = cudaMemsetAsync(tw.nnz, 0, sizeof(int32_t) * (size_t)M, s);
+    const bool tail = gated && decode_tail_ok(M, (F + kGateBM - 1) / kGateBM, tw.n_tiles);
+    // the decode tail derives nnz from the staged counts; the other paths count into it
+    cudaError_t e = tail ? cudaSuccess : cudaMemsetAsync(tw.nnz, 0, sizeof(int32_t) * (size_t)M, s);
     GemmArgs ga{};
     ga.K = d;
     ga.bias = b;
@@ -241,9 +251,23 @@ twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16
         ga.rowsB = M;
         ga.gstage = w.gstage;
         ga.NB = (F + kGateBM - 1) / kGateBM;
+        if (tail) {
+            ga.nnz = nullptr;
+            ga.zero_word = w.counter;
+        }
         timer_begin(TWELL_SITE_UP_GEMM, s);
         if (e == cudaSuccess) e = launch_gemm(GEMM_GATE_SWAP, W_gate, x, ga, sms, s);
         timer_end(TWELL_SITE_UP_GEMM, s);
+        if (tail) {
+            const bool down = W_down && y;
+            timer_begin(TWELL_SITE_DECODE_TAIL, s);
+            if (e == cudaSuccess)
+                e = launch_decode_tail(w.gstage, w.stage_cnt, ga.NB, kGateBM, x, W_up, W_down, d, tw,
+                                       down ? y : nullptr, w.counter, status, s);
+            timer_end(TWELL_SITE_DECODE_TAIL, s);
+            *fused_down = down;
+            return cuda_status(e);
+        }
         if (small_fill_ok(M, ga.NB)) {
             if (e == cudaSuccess)
                 e = launch_layout_fill_small_gate(w.gstage, w.stage_cnt, ga.NB, kGateBM, tw, w.gval, status, s);
@@ -257,13 +281,26 @@ twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16
     return cuda_status(e);
 }
 
+}  // namespace
+
+twell_status twell_up_pack(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b, int M,
+                           int d, int F, int T, const twell_buf* h_out, void* ws, size_t ws_bytes, int32_t* status,
+                           void* stream)
+{
+    bool fused = false;
+    return up_pack_impl(x, W_up, W_gate, b, M, d, F, T, h_out, ws, ws_bytes, status, stream, nullptr, nullptr,
+                        &fused);
+}
+
 twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_gate, const float* b,
                            const uint16_t* W_down, int M, int d, int F, int T, const twell_buf* h_out, uint16_t* y,
                            void* ws, size_t ws_bytes, int32_t* status, void* stream)
 {
     if (!W_down || !y || !aligned16(W_down) || !aligned16(y)) return TWELL_ERR_INVALID_ARG;
-    twell_status st = twell_up_pack(x, W_up, W_gate, b, M, d, F, T, h_out, ws, ws_bytes, status, stream);
-    if (st != TWELL_OK) return st;
+    bool fused = false;
+    twell_status st =
+        up_pack_impl(x, W_up, W_gate, b, M, d, F, T, h_out, ws, ws_bytes, status, stream, W_down, y, &fused);
+    if (st != TWELL_OK || fused) return st;
     const TwellView tw = view_of(h_out);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     timer_begin(TWELL_SITE_SPMM_DOWN, s);
@@ -343,7 +380,7 @@ twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const 
 
 twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end)
 {
-    if (site < TWELL_SITE_NONE || site > TWELL_SITE_WGRAD) return TWELL_ERR_INVALID_ARG;
+    if (site < TWELL_SITE_NONE || site > TWELL_SITE_DECODE_TAIL) return TWELL_ERR_INVALID_ARG;
     g_timer.site = (ev_begin && ev_end) ? site : TWELL_SITE_NONE;
     g_timer.begin = static_cast<cudaEvent_t>(ev_begin);
     g_timer.end = static_cast<cudaEvent_t>(ev_end);

@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncthreads();
     if (*skip) return;  // an earlier kernel of this call failed; uniform over the block
+    if (a.zero_word && blockIdx.x == 0 && threadIdx.x == 0) *a.zero_word = 0;
     if (warp == 1) {
         tmem_alloc(tmem_slot, L::TMEM_COLS);
         tmem_relinquish();
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(192, 1)
                             const int total = __popc(s_mask[t * 4 + 0]) + __popc(s_mask[t * 4 + 1]) +
                                               __popc(s_mask[t * 4 + 2]) + __popc(s_mask[t * 4 + 3]);
                             a.stage_cnt[(size_t)(tok0 + t) * a.NB + mb] = total;
-                            if (total) atomicAdd(&a.nnz[tok0 + t], total);
+                            if (total && a.nnz) atomicAdd(&a.nnz[tok0 + t], total);
                         }
                     }
                 }

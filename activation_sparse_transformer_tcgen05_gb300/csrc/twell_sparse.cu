@@ -149,11 +149,6 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b)
 
 __device__ __forceinline__ uint4 ldg16(const uint16_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
-__device__ __forceinline__ float load_val(const float* vals_f32, const uint16_t* val_bf16, int64_t s)
-{
-    return vals_f32 ? vals_f32[s] : bf16_to_f32(val_bf16[s]);
-}
-
 __device__ __forceinline__ bool over_capacity(const TwellView& tw)
 {
     return tw.off[tw.n_tiles] > tw.cap;
@@ -463,6 +458,238 @@ __global__ void __launch_bounds__(kWarps * 32) k_gated_up_slots(TwellView tw, co
         }
         acc = warp_sum_f(acc);
         if (lane == 0) tw.val[s] = f32_to_bf16_bits(fmaxf(gval[s], 0.f) * acc);
+    }
+}
+
+// ---------------------------------------------------------- decode tail --
+//
+// Everything of the gated forward after the gate GEMM, for decode batches
+// (M <= 64), in one cooperative launch of one 512-thread block per SM. At
+// these sizes each separate kernel costs a launch, a drain and a chain of
+// dependent global round trips while moving well under a megabyte, so:
+//   A. every block reads the staged per-(token, 128-unit block) counts and
+//      computes the TwELL layout (token prefixes, nnz, tile widths, offsets)
+//      in shared memory; block 0 writes nnz / K / off, and each block writes
+//      the padding of its share of the tokens;
+//   B. one warp per active (token, unit) entry, over all warps of the GPU:
+//      u = x[t] . W_up[j], h = bf16(relu(g) * u), written to its slot;
+//   C. after a grid barrier (bounded wait; on expiry the block reports
+//      TWELL_ERR_TIMEOUT and leaves), y[t, 256-column group] = sum over the
+//      token's entries of h * W_down[j, group], split over `split` warps whose
+//      partial sums are added in warp order (deterministic), as in k_spmm_rows.
+// With y == nullptr only A and B run (the TwELL without the down-projection).
+constexpr int kTailWarps = 16;
+constexpr int kTailMaxM = 64;
+constexpr int kTailMaxSeg = 8192;  // M * NB staged segments held in shared memory
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kTailWarps * 32, 1)
+    k_decode_tail(const uint2* __restrict__ gstage, const int32_t* __restrict__ stage_cnt, int NB, int BM,
+                  const uint16_t* __restrict__ x, const uint16_t* __restrict__ W_up,
+                  const uint16_t* __restrict__ W_down, int d, TwellView tw, uint16_t* __restrict__ y, int split,
+                  int32_t* counter, int32_t* status)
+{
+    __shared__ union {
+        int pre[kTailMaxSeg];                 // A, B: exclusive prefix of a token's staged counts
+        float red[kTailWarps][256];           // C: partial sums of split tasks
+    } sm;
+    __shared__ int s_nnz[kTailMaxM], s_tok[kTailMaxM + 1], s_K[kTailMaxM];
+    __shared__ long long s_off[kTailMaxM + 1];
+    __shared__ int s_go;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int M = tw.M, nseg = M * NB;
+    if (has_error(status)) return;
+
+    // ---------------------------------------------------------------- A --
+    for (int i = tid; i < nseg; i += blockDim.x) sm.pre[i] = stage_cnt[i];
+    __syncthreads();
+    for (int t = warp; t < M; t += kTailWarps) {
+        int carry = 0;
+        for (int nb0 = 0; nb0 < NB; nb0 += 32) {
+            const int nb = nb0 + lane;
+            const int c = nb < NB ? sm.pre[t * NB + nb] : 0;
+            const int incl = warp_incl_scan(c, lane);
+            if (nb < NB) sm.pre[t * NB + nb] = carry + incl - c;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s_nnz[t] = carry;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        long long off = 0;
+        for (int tt = 0; tt < tw.n_tiles; ++tt) {
+            const int r0 = tt * tw.T, rows = min(tw.T, M - r0);
+            int mx = 0;
+            for (int i = 0; i < rows; ++i) mx = max(mx, s_nnz[r0 + i]);
+            s_K[tt] = mx;
+            s_off[tt] = off;
+            off += (long long)rows * mx;
+        }
+        s_off[tw.n_tiles] = off;
+        int e = 0;
+        for (int t = 0; t < M; ++t) {
+            s_tok[t] = e;
+            e += s_nnz[t];
+        }
+        s_tok[M] = e;
+    }
+    __syncthreads();
+    const bool over = s_off[tw.n_tiles] > tw.cap;
+    if (blockIdx.x == 0) {
+        for (int t = tid; t < M; t += blockDim.x) tw.nnz[t] = s_nnz[t];
+        for (int tt = tid; tt <= tw.n_tiles; tt += blockDim.x) {
+            if (tt < tw.n_tiles) tw.K[tt] = s_K[tt];
+            tw.off[tt] = s_off[tt];
+        }
+        if (tid == 0 && over) set_error(status, TWELL_ERR_CAPACITY);
+    }
+    if (over) return;  // uniform: every block computed the same layout
+    for (int t = blockIdx.x + warp * gridDim.x; t < M; t += gridDim.x * kTailWarps) {
+        const int tt = t / tw.T;
+        const long long base = s_off[tt] + (long long)(t - tt * tw.T) * s_K[tt];
+        for (int k = s_nnz[t] + lane; k < s_K[tt]; k += 32) {
+            tw.idx[base + k] = -1;
+            tw.val[base + k] = 0;
+        }
+    }
+
+    // ---------------------------------------------------------------- B --
+    const int E = s_tok[M];
+    const int nwarps = gridDim.x * kTailWarps;
+    for (int e = blockIdx.x * kTailWarps + warp; e < E; e += nwarps) {
+        int lo = 0, hi = M;  // token: last t with s_tok[t] <= e
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_tok[mid] <= e) lo = mid; else hi = mid;
+        }
+        const int t = lo, k = e - s_tok[t];
+        const int* pre = sm.pre + t * NB;
+        int a = 0, b = NB;  // staged segment: last nb with pre[nb] <= k
+        while (b - a > 1) {
+            const int mid = (a + b) >> 1;
+            if (pre[mid] <= k) a = mid; else b = mid;
+        }
+        const uint2 ent = gstage[((size_t)t * NB + a) * BM + (k - pre[a])];
+        const int j = (int)ent.x;
+        const uint16_t* xr = x + (size_t)t * d + lane * 8;
+        const uint16_t* wr = W_up + (size_t)j * d + lane * 8;
+        float acc = 0.f;
+        for (int c0 = 0; c0 < d; c0 += 8 * 256) {
+            uint4 av[8], wv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int c = c0 + q * 256;
+                const bool ok = c + lane * 8 < d;
+                av[q] = ok ? ldg16(xr + c) : make_uint4(0, 0, 0, 0);
+                wv[q] = ok ? ldg16(wr + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc += dot8_bf16(av[q], wv[q]);
+        }
+        acc = warp_sum_f(acc);
+        if (lane == 0) {
+            const int tt = t / tw.T;
+            const long long slot = s_off[tt] + (long long)(t - tt * tw.T) * s_K[tt] + k;
+            tw.idx[slot] = j;
+            tw.val[slot] = f32_to_bf16_bits(fmaxf(__uint_as_float(ent.y), 0.f) * acc);
+        }
+    }
+    if (!y) return;
+
+    // ------------------------------------------------------ grid barrier --
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        atomicAdd(counter, 1);
+        const uint64_t t0 = globaltimer_ns();
+        int go = 1;
+        while (ld_acquire_gpu(counter) < (int)gridDim.x) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                go = 0;
+                break;
+            }
+        }
+        s_go = go;
+    }
+    __syncthreads();
+    if (!s_go) {
+        if (tid == 0) set_error(status, TWELL_ERR_TIMEOUT);
+        return;
+    }
+
+    // ---------------------------------------------------------------- C --
+    const int G = (d + 255) >> 8;
+    const long long tasks = (long long)M * G;
+    const int tpb = kTailWarps / split;  // tasks per block and round
+    const int sub = warp % split;
+    for (long long t0 = (long long)blockIdx.x * tpb; t0 < tasks; t0 += (long long)gridDim.x * tpb) {
+        const long long task = t0 + warp / split;
+        const bool task_ok = task < tasks;
+        const int t = task_ok ? (int)(task / G) : 0, g = task_ok ? (int)(task % G) : 0;
+        const int c0 = g * 256 + lane * 8;
+        const bool col_ok = task_ok && c0 < d;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        if (task_ok) {
+            const int tt = t / tw.T;
+            const long long base = s_off[tt] + (long long)(t - tt * tw.T) * s_K[tt];
+            const int n = s_nnz[t];
+            const int per = (n + split - 1) / split;
+            const int kb = min(n, sub * per), ke = min(n, kb + per);
+            const uint16_t* Wc = W_down + c0;
+            for (int k0 = kb; k0 < ke; k0 += 32) {
+                const int m = min(32, ke - k0);
+                int jl = 0;
+                uint32_t vb = 0;
+                if (lane < m) {
+                    jl = __ldcg(tw.idx + base + k0 + lane);
+                    vb = __ldcg(tw.val + base + k0 + lane);
+                }
+                int u = 0;
+                for (; u + 4 <= m; u += 4) {
+                    uint4 w[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int jj = __shfl_sync(0xffffffffu, jl, u + q);
+                        w[q] = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) fma8_bf16(acc, __shfl_sync(0xffffffffu, vb, u + q), w[q]);
+                }
+                for (; u < m; ++u) {
+                    const int jj = __shfl_sync(0xffffffffu, jl, u);
+                    const uint4 w = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
+                    fma8_bf16(acc, __shfl_sync(0xffffffffu, vb, u), w);
+                }
+            }
+        }
+        if (split > 1) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sm.red[warp][lane * 8 + e] = acc[e];
+            __syncthreads();
+            if (sub == 0) {
+                for (int s2 = 1; s2 < split; ++s2) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] += sm.red[warp + s2][lane * 8 + e];
+                }
+            }
+        }
+        if (sub == 0 && col_ok) {
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(y + (size_t)t * d + c0) = o;
+        }
+        if (split > 1) __syncthreads();  // red is rewritten in the next round
     }
 }
 
@@ -999,6 +1226,55 @@ cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16
 }
 
 bool small_fill_ok(int M, int NB) { return M <= 1024 && (long long)M * NB <= kSmallFillMax; }
+
+int decode_tail_grid()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_tail, kTailWarps * 32, 0) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            cached[dev] = -1;
+        } else {
+            cached[dev] = per_sm >= 1 ? sms : -1;
+        }
+    }
+    return cached[dev];
+}
+
+bool decode_tail_ok(int M, int NB, int n_tiles)
+{
+    return M <= kTailMaxM && (long long)M * NB <= kTailMaxSeg && n_tiles <= kTailMaxM && decode_tail_grid() > 0;
+}
+
+cudaError_t launch_decode_tail(const uint2* gstage, const int32_t* stage_cnt, int NB, int BM, const uint16_t* x,
+                               const uint16_t* W_up, const uint16_t* W_down, int d, const TwellView& tw,
+                               uint16_t* y, int32_t* counter, int32_t* status, cudaStream_t s)
+{
+    const int grid = decode_tail_grid();
+    if (grid <= 0) return cudaErrorInvalidConfiguration;
+    // warps per down-projection task: as many as keep every warp of the grid busy
+    const long long tasks = (long long)tw.M * ((d + 255) / 256);
+    int split = kTailWarps;
+    while (split > 1 && tasks * split > (long long)grid * kTailWarps) split >>= 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all blocks resident: the grid barrier can complete
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kTailWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    count_launches(1);
+    return cudaLaunchKernelEx(&cfg, k_decode_tail, gstage, stage_cnt, NB, BM, x, W_up, W_down, d, tw, y, split,
+                              counter, status);
+}
 
 cudaError_t launch_layout_fill_small_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
                                           const TwellView& tw, float* gval, int32_t* status, cudaStream_t s)

@@ -28,7 +28,7 @@ EXPORTED_SYMBOLS = (
 )
 
 # Call sites of twell_set_kernel_timer.
-SITE_NONE, SITE_UP_GEMM, SITE_SPMM_DOWN, SITE_SDDMM, SITE_DX, SITE_CSC, SITE_WGRAD = range(7)
+SITE_NONE, SITE_UP_GEMM, SITE_SPMM_DOWN, SITE_SDDMM, SITE_DX, SITE_CSC, SITE_WGRAD, SITE_DECODE_TAIL = range(8)
 
 # Size of the library-owned workspace behind twell_ffn_fwd_static_ws.
 STATIC_WS_BYTES = 32 * 1024 * 1024

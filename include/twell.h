@@ -222,9 +222,11 @@ twell_status twell_ffn_fwd_static_ws(const uint16_t* x, const uint16_t* W_up, co
  *   3 backward SDDMM            4 backward dx
  *   5 backward column lists (first to last of its kernels)
  *   6 backward weight gradients
+ *   7 gated decode tail (M <= 64: layout, gated up products and, in
+ *     twell_ffn_fwd, the down-projection, in one launch)
  */
 enum { TWELL_SITE_NONE = 0, TWELL_SITE_UP_GEMM = 1, TWELL_SITE_SPMM_DOWN = 2, TWELL_SITE_SDDMM = 3,
-       TWELL_SITE_DX = 4, TWELL_SITE_CSC = 5, TWELL_SITE_WGRAD = 6 };
+       TWELL_SITE_DX = 4, TWELL_SITE_CSC = 5, TWELL_SITE_WGRAD = 6, TWELL_SITE_DECODE_TAIL = 7 };
 twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end);
 
 /* Number of kernels this library has launched in this process (host-side
