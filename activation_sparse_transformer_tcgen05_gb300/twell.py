@@ -24,7 +24,7 @@ EXPORTED_SYMBOLS = (
     "twell_status_string", "twell_buf_slots_bound", "twell_workspace_bytes", "twell_device_sm_count",
     "twell_pack", "twell_up_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd",
     "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
-    "twell_set_kernel_timer",
+    "twell_set_kernel_timer", "twell_gather_probe",
 )
 
 # Call sites of twell_set_kernel_timer.
@@ -86,6 +86,8 @@ def load_library(path: str | None = None):
     lib.twell_dense_ffn_fwd.argtypes = [P, P, P, P, I32, I32, I32, P, P, P, P]
     lib.twell_ffn_fwd_static_ws.restype = I32
     lib.twell_ffn_fwd_static_ws.argtypes = [P, P, P, P, P, I32, I32, I32, I32, BUFP, P, P, P]
+    lib.twell_gather_probe.restype = I32
+    lib.twell_gather_probe.argtypes = [P, I32, I32, P, I32, I32, P, P]
     lib.twell_check.restype = I32
     lib.twell_check.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     _lib = lib
@@ -180,6 +182,17 @@ def twell_set_kernel_timer(site: int, ev_begin=None, ev_end=None):
     b = ctypes.c_void_p(ev_begin.cuda_event) if ev_begin is not None else None
     e = ctypes.c_void_p(ev_end.cuda_event) if ev_end is not None else None
     _check(load_library().twell_set_kernel_timer(int(site), b, e), "twell_set_kernel_timer")
+
+
+def twell_gather_probe(W: torch.Tensor, idx: torch.Tensor, sink: torch.Tensor, stream=None):
+    """The sparse kernels' row-gather access pattern alone (measurement aid):
+    W [F, d] bf16 bits, idx [rows, nnz] int32, sink [rows * ceil(d/256)] float32."""
+    F, d = W.shape
+    rows, nnz = idx.shape
+    _check(load_library().twell_gather_probe(
+        _ptr(W, "W", bytes_per_elem=2, numel=F * d), F, d, _ptr(idx, "idx", bytes_per_elem=4, numel=rows * nnz),
+        rows, nnz, _ptr(sink, "sink", bytes_per_elem=4, numel=rows * ((d + 255) // 256)), _stream(stream)),
+        "twell_gather_probe")
 
 
 def twell_up_pack(x, W_up, W_gate, b, T: int, h_out: TwellBuffers, ws, status, stream=None):

@@ -20,6 +20,7 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -224,6 +225,33 @@ def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:
     return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
+# call site's kernel on this workload, from one `ncu --set full` capture, with
+# the SHA-256 of the source file it was built from: once that file changes the
+# figure no longer describes the kernel and the site reports traffic null.
+NCU_TRAFFIC = {
+    1: ("twell_gemm.cu", "50c5bcbe297020cb5efca65ef6baf81f8ed87f8fe9ee17c4ebabec69edf5b5c6", 54.121472e6),
+    2: ("twell_sparse.cu", "fb3f9a65de8402ef8c0b4474b2c480db522c71588943ad2fae358de60823d6f8", 37.864704e6),
+    3: ("twell_sparse.cu", "fb3f9a65de8402ef8c0b4474b2c480db522c71588943ad2fae358de60823d6f8", 52.628224e6),
+    4: ("twell_sparse.cu", "fb3f9a65de8402ef8c0b4474b2c480db522c71588943ad2fae358de60823d6f8", 38.702592e6),
+    6: ("twell_sparse.cu", "fb3f9a65de8402ef8c0b4474b2c480db522c71588943ad2fae358de60823d6f8", 136.318464e6),
+}
+
+
+def ncu_traffic(site: int, workload: str):
+    ent = NCU_TRAFFIC.get(site)
+    if ent is None or workload != CONFIG_NAME:
+        return None
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "activation_sparse_transformer_tcgen05_gb300",
+                        "csrc", ent[0])
+    try:
+        with open(path, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return ent[2] if digest == ent[1] else None
+
+
 def kernel_roofline(site: int, us: float, inp, slots: int, nnz: int, peaks, fp32_peak: float):
     """Roofline of one kernel call site: bound, achieved, peak, unit, frac (traffic filled from ncu)."""
     M, d, F = inp.M, inp.d, inp.F
@@ -232,7 +260,8 @@ def kernel_roofline(site: int, us: float, inp, slots: int, nnz: int, peaks, fp32
         flops = 2.0 * M * d * F
         a = flops / s / 1e12
         return {"bound": "tensor", "achieved": a, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                "frac": a / peaks["bf16"], "traffic": None, "algorithmic": f"{flops / 1e9:.1f} GFLOP"}
+                "frac": a / peaks["bf16"], "traffic": ncu_traffic(site, CONFIG_NAME),
+                "algorithmic": f"{flops / 1e9:.1f} GFLOP"}
     if site == 5:
         by = slots * (4 + 2 + 4) + nnz * (4 + 2 + 4 + 8) + F * 8
         a = by / s / 1e9
@@ -241,7 +270,48 @@ def kernel_roofline(site: int, us: float, inp, slots: int, nnz: int, peaks, fp32
     flops = 2.0 * nnz * d * (2 if site == 6 else 1)
     a = flops / s / 1e12
     return {"bound": "alu", "achieved": a, "peak": fp32_peak, "unit": "TFLOP/s", "frac": a / fp32_peak,
-            "traffic": None, "algorithmic": f"{flops / 1e9:.2f} GFLOP fp32 FMA on stored entries"}
+            "traffic": ncu_traffic(site, CONFIG_NAME),
+            "algorithmic": f"{flops / 1e9:.2f} GFLOP fp32 FMA on stored entries"}
+
+
+# Bytes each gather kernel pulls through L2 per stored entry, in rows of d bf16:
+# down-projection and SDDMM a W_down row, dx a W_up row, weight gradients an x
+# row and a dy row.
+GATHER_ROWS = {2: 1, 3: 1, 4: 1, 6: 2}
+
+
+def gather_ceiling(tw, W, nnz_per_row: int, reps: int = 10):
+    """Measured rate (TB/s) of the sparse kernels' access pattern alone: warps
+    gathering 512-byte stretches of random rows of W (L2-resident) with
+    128-bit loads (twell_gather_probe), best of `reps` after warm-up."""
+    F, d = W.shape
+    rows = 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    idx = torch.randint(0, F, (rows, nnz_per_row), dtype=torch.int32, device="cuda", generator=g)
+    sink = torch.empty(rows * ((d + 255) // 256), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        tw.twell_gather_probe(W, idx, sink)
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        tw.twell_gather_probe(W, idx, sink)
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    best = min(a.elapsed_time(b) for a, b in ts) * 1e-3
+    return rows * nnz_per_row * d * 2 / best / 1e12
+
+
+def gather_roofline(site: int, us: float, nnz: int, d: int, ceiling_tbs: float):
+    if site not in GATHER_ROWS:
+        return None
+    by = GATHER_ROWS[site] * nnz * d * 2
+    a = by / (us * 1e-6) / 1e12
+    return {"achieved_TBs": a, "ceiling_TBs": ceiling_tbs, "frac": a / ceiling_tbs,
+            "bytes_gathered": by, "ceiling_source": "twell_gather_probe, same run"}
 
 
 def stage_roofline(name, ms, inp, slots, nnz, peaks):
@@ -441,10 +511,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     roof["us_per_launch"] = dom_us
     roof["peak_source"] = (f"{peaks['src']} (MEASURED_PEAKS.json)" if roof["bound"] != "alu" else
                            f"derived: {tw.twell_device_sm_count()} SMs x 128 FMA/clk x 2 x {peaks['sm_max_mhz']:.0f} MHz")
-    kernels = {SITES[k]: dict(us=v, **{q: r for q, r in kernel_roofline(k, v, inp, slots, nnz, peaks,
-                                                                         fp32_peak).items()
-                                        if q in ("bound", "achieved", "unit", "frac")})
-               for k, v in site_us.items()}
+    ceiling = gather_ceiling(tw, L.Wd.view(inp.F, inp.d), max(1, round(nnz / inp.M)))
+    g_dom = gather_roofline(dom_site, dom_us, nnz, inp.d, ceiling)
+    if g_dom:
+        roof["l2_gather"] = g_dom
+    kernels = {}
+    for k, v in site_us.items():
+        kr = kernel_roofline(k, v, inp, slots, nnz, peaks, fp32_peak)
+        kernels[SITES[k]] = dict(us=v, **{q: r for q, r in kr.items()
+                                          if q in ("bound", "achieved", "unit", "frac", "traffic")})
+        gk = gather_roofline(k, v, nnz, inp.d, ceiling)
+        if gk:
+            kernels[SITES[k]]["l2_gather_frac"] = gk["frac"]
 
     # ---- end to end through the public API with host buffers
     e2e = None

@@ -229,6 +229,24 @@ enum { TWELL_SITE_NONE = 0, TWELL_SITE_UP_GEMM = 1, TWELL_SITE_SPMM_DOWN = 2, TW
        TWELL_SITE_DX = 4, TWELL_SITE_CSC = 5, TWELL_SITE_WGRAD = 6, TWELL_SITE_DECODE_TAIL = 7 };
 twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end);
 
+/*
+ * twell_gather_probe — measurement aid: the memory access pattern of the
+ * library's sparse kernels without their arithmetic, so that their time can be
+ * set against the gather rate of the GPU they run on. One warp per (row r,
+ * 256-column group g) reads, for k < nnz, the 16 bytes of W[idx[r*nnz + k]]
+ * at columns 256 g + 8 lane .. +7 (eight 128-bit loads per lane in flight)
+ * and writes one checksum float per task to sink.
+ *   W    [F, d] bf16 row-major, device, 16-byte aligned, d a multiple of 8
+ *   idx  [rows, nnz] int32, device; values are clamped into [0, F)
+ *   sink [rows * ceil(d/256)] float, device, written
+ * Bytes gathered per call: rows * nnz * d * 2. Asynchronous on `stream`.
+ * Errors: TWELL_ERR_INVALID_ARG (null pointer, non-positive F/d/rows, negative
+ * nnz, d % 8 != 0, W misaligned), TWELL_ERR_UNSUPPORTED (grid too large),
+ * TWELL_ERR_CUDA (launch failed).
+ */
+twell_status twell_gather_probe(const uint16_t* W, int F, int d, const int32_t* idx, int rows, int nnz, float* sink,
+                                void* stream);
+
 /* Number of kernels this library has launched in this process (host-side
  * counter, all devices). Lets a caller count the library's launches in a
  * timed region. */

@@ -387,3 +387,23 @@ def test_fwd_skewed_rows(name):
     assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], ref["y"], what="y rows", bf16_out=True)
     # skew makes the widest row of a tile several times its mean
     assert got.K.max() > 2 * got.nnz.mean()
+
+
+def test_gather_probe_reads_the_named_rows():
+    # the gather-ceiling probe must touch exactly W[idx[r, k], 256 g + 8 lane .. +7]:
+    # its per-task checksum (xor of every 32-bit word read, 23 low bits) is recomputed here
+    F, d, rows, nnz = 300, 520, 37, 45
+    rng = np.random.default_rng(5)
+    W = rng.integers(-32768, 32767, size=(F, d), dtype=np.int16)
+    idx = rng.integers(0, F, size=(rows, nnz), dtype=np.int32)
+    G = (d + 255) // 256
+    sink = torch.empty(rows * G, dtype=torch.float32, device="cuda")
+    tw.twell_gather_probe(torch.from_numpy(W).cuda(), torch.from_numpy(idx).cuda(), sink)
+    got = sink.cpu().numpy().view(np.uint32)
+    words = W.view(np.uint32).reshape(F, d // 2)
+    want = np.zeros(rows * G, dtype=np.uint32)
+    for r in range(rows):
+        for g in range(G):
+            c = words[idx[r], g * 128:min((g + 1) * 128, d // 2)]
+            want[r * G + g] = np.bitwise_xor.reduce(c.reshape(-1)) & 0x007fffff
+    np.testing.assert_array_equal(got, want)
