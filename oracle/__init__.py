@@ -152,6 +152,20 @@ def twell_pack(h: np.ndarray, T: int, active: np.ndarray | None = None) -> Twell
     return Twell(M, F, T, nnz, K, off, idx[:total].copy(), val[:total].copy())
 
 
+def hybrid_pack(h: np.ndarray, T: int, C: int) -> tuple[Twell, np.ndarray, np.ndarray]:
+    """Hybrid format of a dense [M, F] bf16 matrix ("Sparser, Faster, Lighter
+    Transformer Language Models", Resumo Técnico §2, "Formato Híbrido para
+    Treinamento"): a row with more than C nonzeros (+-0 are zeros) overflows.
+    Returns (TwELL of h with the overflow rows emptied, overflow row ids
+    ascending, their dense rows [n, F])."""
+    h = _c(h, np.uint16)
+    counts = ((h & 0x7FFF) != 0).sum(axis=1)
+    rows = np.nonzero(counts > C)[0].astype(np.int32)
+    h_ell = h.copy()
+    h_ell[rows] = 0
+    return twell_pack(h_ell, T), rows, h[rows].copy()
+
+
 def twell_unpack(tw: Twell) -> tuple[int, np.ndarray]:
     """(status, dense h). status 0 = valid TwELL; see the C comment for codes."""
     h = np.empty((tw.M, tw.F), np.uint16)

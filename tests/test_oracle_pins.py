@@ -148,6 +148,48 @@ def test_pack_special_cases():
     assert tw0.slots == 0 and (tw0.K == 0).all()
 
 
+@pytest.mark.parametrize("M,F,T,density,C,seed", [
+    (30, 40, 4, 0.15, 5, 1), (25, 64, 8, 0.1, 0, 2), (18, 33, 100, 0.3, 33, 3), (40, 50, 1, 0.08, 3, 4)])
+def test_hybrid_pack_matches_brute_force(M, F, T, density, C, seed):
+    # skewed rows so that some overflow and some do not
+    h = syn.sparse_hidden(M, F, density, seed=seed, row_skew_sigma=1.0)
+    tw, rows, dense = oracle.hybrid_pack(h, T, C)
+    # brute force: python loops over the rows
+    over, kept = [], h.copy()
+    for r in range(M):
+        n = sum(1 for j in range(F) if int(h[r, j]) & 0x7FFF)
+        if n > C:
+            over.append(r)
+            kept[r, :] = 0
+    assert rows.tolist() == over
+    np.testing.assert_array_equal(dense, h[over] if over else np.zeros((0, F), np.uint16))
+    nnz, K, off, idx, val = _brute_twell(kept, T)
+    np.testing.assert_array_equal(tw.nnz, nnz)
+    np.testing.assert_array_equal(tw.K, K)
+    np.testing.assert_array_equal(tw.idx, np.array(idx, np.int32))
+    np.testing.assert_array_equal(tw.val, np.array(val, np.uint16))
+    assert (tw.K <= C).all()
+    # the two parts together give h back
+    code, back = oracle.twell_unpack(tw)
+    assert code == 0
+    back[rows] = dense
+    np.testing.assert_array_equal(back, np.where(h == 0x8000, np.uint16(0), h))
+
+
+def test_hybrid_pack_special_cases():
+    M, F = 20, 30
+    h = syn.sparse_hidden(M, F, 0.2, seed=8)
+    # capacity F: nothing overflows, the TwELL part is the plain TwELL
+    tw, rows, dense = oracle.hybrid_pack(h, 4, F)
+    ref = oracle.twell_pack(h, 4)
+    assert rows.size == 0 and dense.shape == (0, F)
+    np.testing.assert_array_equal(tw.idx, ref.idx)
+    np.testing.assert_array_equal(tw.val, ref.val)
+    # capacity 0: every nonempty row overflows and the TwELL part is empty
+    tw0, rows0, dense0 = oracle.hybrid_pack(h, 4, 0)
+    assert tw0.slots == 0 and rows0.tolist() == np.flatnonzero(((h & 0x7FFF) != 0).any(1)).tolist()
+
+
 def test_unpack_rejects_malformed():
     h = syn.sparse_hidden(10, 20, 0.3, seed=9)
     tw = oracle.twell_pack(h, 4)
