@@ -47,8 +47,16 @@ cudaError_t launch_tile_layout(const TwellView& tw, int32_t* status, cudaStream_
 cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, int32_t* status, cudaStream_t s);
 // Slots from GEMM-epilogue staging. ReLU staging: uint32 (bf16 << 16 | local col);
 // gate staging: uint2 (global col, fp32 gate bits) and gate values go to gval[slot].
+// ov_pos (hybrid format, else null): rows with ov_pos[r] >= 0 are left empty.
 cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
-                                    const TwellView& tw, int32_t* status, cudaStream_t s);
+                                    const TwellView& tw, const int32_t* ov_pos, int32_t* status, cudaStream_t s);
+// Hybrid format: overflow rows (nnz > C) in ascending order, nnz of those rows
+// set to 0 (run before launch_tile_layout), then their dense hidden rows.
+cudaError_t launch_overflow_rows(const TwellView& tw, int C, int cap_rows, int32_t* ov_pos, int32_t* ov_rows,
+                                 int32_t* n_rows, int32_t* status, cudaStream_t s);
+cudaError_t launch_overflow_dense(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN, int F,
+                                  const int32_t* ov_rows, const int32_t* n_rows, int cap_rows, uint16_t* dense,
+                                  const int32_t* status, cudaStream_t s);
 cudaError_t launch_fill_staged_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
                                     const TwellView& tw, float* gval, int32_t* status, cudaStream_t s);
 
@@ -107,6 +115,8 @@ struct GemmArgs {
     int32_t* stage_cnt;    // [rows, NB]
     int32_t* nnz;          // [rows], zeroed by the caller before the launch; null: not counted
     int32_t* zero_word;    // if set, written 0 by the kernel (a counter the next kernel starts from)
+    const int32_t* rowsA_dev;  // if set, rows of A actually used: min(*rowsA_dev, rowsA), read on the device
+    const int32_t* row_map;    // DENSE only: if set, output row of A's row i is row_map[i]
     int NB;                // column blocks of the staging
     uint16_t* out;         // DENSE output [rowsA, ldo]
     int ldo;

@@ -51,9 +51,10 @@ struct FwdWs {
     uint2* gstage;
     float* gval;
     int32_t* counter;  // grid-barrier counter of the gated decode tail
+    int32_t* ov_pos;   // hybrid: position of row r in the overflow block, or -1
 };
 
-size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out)
+size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out, bool hybrid = false)
 {
     Carver c{static_cast<char*>(ws)};
     FwdWs w{};
@@ -61,6 +62,7 @@ size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out)
         const size_t NB = (F + kReluBN - 1) / kReluBN;
         w.stage_cnt = c.take<int32_t>((size_t)M * NB);
         w.stage = c.take<uint32_t>((size_t)M * NB * kReluBN);
+        if (hybrid) w.ov_pos = c.take<int32_t>((size_t)M);
     } else {
         const size_t NB = (F + kGateBM - 1) / kGateBM;
         w.stage_cnt = c.take<int32_t>((size_t)M * NB);
@@ -160,6 +162,7 @@ size_t twell_workspace_bytes(int op, int M, int d, int F, int T, int64_t cap_slo
         case TWELL_OP_FFN_FWD: return carve_fwd(nullptr, false, M, F, cap_slots, nullptr);
         case TWELL_OP_GATED_FWD: return carve_fwd(nullptr, true, M, F, cap_slots, nullptr);
         case TWELL_OP_FFN_BWD: return carve_bwd(nullptr, M, F, cap_slots, nullptr);
+        case TWELL_OP_HYBRID_FWD: return carve_fwd(nullptr, false, M, F, cap_slots, nullptr, true);
         default: return 0;
     }
 }
@@ -244,7 +247,7 @@ twell_status up_pack_impl(const uint16_t* x, const uint16_t* W_up, const uint16_
             if (e == cudaSuccess) e = launch_layout_fill_small_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, status, s);
         } else {
             if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
-            if (e == cudaSuccess) e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, status, s);
+            if (e == cudaSuccess) e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, nullptr, status, s);
         }
     } else {
         ga.rowsA = F;
@@ -307,6 +310,99 @@ twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16
     const cudaError_t e = launch_spmm_rows(tw, nullptr, W_down, d, y, status, s);
     timer_end(TWELL_SITE_SPMM_DOWN, s);
     return cuda_status(e);
+}
+
+// ----------------------------------------------------------------- hybrid --
+
+namespace {
+
+bool overflow_ok(const twell_overflow* ov, int F)
+{
+    if (!ov || ov->C < 0 || ov->cap_rows < 0 || !ov->n_rows) return false;
+    if (ov->cap_rows > 0 && (!ov->rows || !ov->dense || !aligned16(ov->dense))) return false;
+    (void)F;
+    return true;
+}
+
+}  // namespace
+
+twell_status twell_hybrid_up_pack(const uint16_t* x, const uint16_t* W_up, const float* b, int M, int d, int F,
+                                  int T, const twell_buf* h_out, const twell_overflow* ov, void* ws,
+                                  size_t ws_bytes, int32_t* status, void* stream)
+{
+    if (!x || !W_up || !b || !status || !dims_ok(M, d, F) || !overflow_ok(ov, F)) return TWELL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W_up)) return TWELL_ERR_INVALID_ARG;
+    twell_status st = check_buf(h_out, M, F, T);
+    if (st != TWELL_OK) return st;
+    const size_t need = carve_fwd(nullptr, false, M, F, h_out->cap_slots, nullptr, true);
+    if (!ws || ws_bytes < need) return TWELL_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;
+    const int sms = sm_count_current();
+    if (sms <= 0) return TWELL_ERR_CUDA;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const TwellView tw = view_of(h_out);
+    FwdWs w;
+    carve_fwd(ws, false, M, F, h_out->cap_slots, &w, true);
+    cudaError_t e = cudaMemsetAsync(tw.nnz, 0, sizeof(int32_t) * (size_t)M, s);
+    GemmArgs ga{};
+    ga.K = d;
+    ga.bias = b;
+    ga.stage_cnt = w.stage_cnt;
+    ga.nnz = tw.nnz;
+    ga.status = status;
+    ga.rowsA = M;
+    ga.rowsB = F;
+    ga.stage = w.stage;
+    ga.NB = (F + kReluBN - 1) / kReluBN;
+    timer_begin(TWELL_SITE_UP_GEMM, s);
+    if (e == cudaSuccess) e = launch_gemm(GEMM_TWELL_RELU, x, W_up, ga, sms, s);
+    timer_end(TWELL_SITE_UP_GEMM, s);
+    if (e == cudaSuccess)
+        e = launch_overflow_rows(tw, ov->C, ov->cap_rows, w.ov_pos, ov->rows, ov->n_rows, status, s);
+    if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
+    if (e == cudaSuccess) e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, w.ov_pos, status, s);
+    if (e == cudaSuccess)
+        e = launch_overflow_dense(w.stage, w.stage_cnt, ga.NB, kReluBN, F, ov->rows, ov->n_rows, ov->cap_rows,
+                                  ov->dense, status, s);
+    return cuda_status(e);
+}
+
+twell_status twell_hybrid_spmm_down(const twell_buf* h, const twell_overflow* ov, const uint16_t* W_down,
+                                    const uint16_t* W_downT, int d, uint16_t* y, int32_t* status, void* stream)
+{
+    if (!h || !W_downT || !aligned16(W_downT) || !overflow_ok(ov, h->F)) return TWELL_ERR_INVALID_ARG;
+    twell_status st = twell_spmm_down(h, W_down, d, y, status, stream);
+    if (st != TWELL_OK || ov->cap_rows == 0) return st;
+    const int sms = sm_count_current();
+    if (sms <= 0) return TWELL_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmArgs g{};
+    g.rowsA = ov->cap_rows;  // upper bound; the kernel reads the actual count
+    g.rowsA_dev = ov->n_rows;
+    g.row_map = ov->rows;
+    g.rowsB = d;
+    g.K = h->F;
+    g.bias = nullptr;
+    g.relu = 0;
+    g.out = y;
+    g.ldo = d;
+    g.status = status;
+    timer_begin(TWELL_SITE_OVERFLOW_GEMM, s);
+    const cudaError_t e = launch_gemm(GEMM_DENSE, ov->dense, W_downT, g, sms, s);
+    timer_end(TWELL_SITE_OVERFLOW_GEMM, s);
+    return cuda_status(e);
+}
+
+twell_status twell_hybrid_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const float* b, const uint16_t* W_down,
+                                  const uint16_t* W_downT, int M, int d, int F, int T, const twell_buf* h_out,
+                                  const twell_overflow* ov, uint16_t* y, void* ws, size_t ws_bytes,
+                                  int32_t* status, void* stream)
+{
+    if (!W_down || !W_downT || !y) return TWELL_ERR_INVALID_ARG;
+    twell_status st = twell_hybrid_up_pack(x, W_up, b, M, d, F, T, h_out, ov, ws, ws_bytes, status, stream);
+    if (st != TWELL_OK) return st;
+    return twell_hybrid_spmm_down(h_out, ov, W_down, W_downT, d, y, status, stream);
 }
 
 twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down, const twell_buf* h,
@@ -380,7 +476,7 @@ twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const 
 
 twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end)
 {
-    if (site < TWELL_SITE_NONE || site > TWELL_SITE_DECODE_TAIL) return TWELL_ERR_INVALID_ARG;
+    if (site < TWELL_SITE_NONE || site > TWELL_SITE_OVERFLOW_GEMM) return TWELL_ERR_INVALID_ARG;
     g_timer.site = (ev_begin && ev_end) ? site : TWELL_SITE_NONE;
     g_timer.begin = static_cast<cudaEvent_t>(ev_begin);
     g_timer.end = static_cast<cudaEvent_t>(ev_end);

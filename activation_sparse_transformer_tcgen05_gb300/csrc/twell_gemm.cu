@@ -107,6 +107,7 @@ __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int nb, c
                                               const float* bias_sm)
 {
     const bool row_ok = row < a.rowsA;
+    const int orow = (row_ok && a.row_map) ? a.row_map[row] : row;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t v[32];
@@ -127,7 +128,7 @@ __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int nb, c
                     o.y = pack_bf16x2(f[2], f[3]);
                     o.z = pack_bf16x2(f[4], f[5]);
                     o.w = pack_bf16x2(f[6], f[7]);
-                    *reinterpret_cast<uint4*>(a.out + (size_t)row * a.ldo + col) = o;
+                    *reinterpret_cast<uint4*>(a.out + (size_t)orow * a.ldo + col) = o;
                 }
             }
         }
@@ -136,8 +137,9 @@ __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int nb, c
 
 template <int BN, int MODE, int STAGES>
 __global__ void __launch_bounds__(192, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs a, int tok0)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs args, int tok0)
 {
+    GemmArgs a = args;
     using L = Layout<BN, STAGES>;
     constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
     extern __shared__ uint8_t smem_raw[];
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     if (*skip) return;  // an earlier kernel of this call failed; uniform over the block
     if (a.zero_word && blockIdx.x == 0 && threadIdx.x == 0) *a.zero_word = 0;
+    if (a.rowsA_dev) a.rowsA = min(*a.rowsA_dev, a.rowsA);  // written by an earlier kernel
     if (warp == 1) {
         tmem_alloc(tmem_slot, L::TMEM_COLS);
         tmem_relinquish();
@@ -400,8 +403,9 @@ struct PairLayout {
 
 template <int MODE, int STAGES>
 __global__ void __launch_bounds__(192, 1)
-    k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs a)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs args)
 {
+    GemmArgs a = args;
     static_assert(MODE == GEMM_TWELL_RELU || MODE == GEMM_DENSE, "row-wise epilogues only");
     using L = PairLayout<STAGES>;
     constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, PAIR_N);
@@ -443,6 +447,7 @@ __global__ void __launch_bounds__(192, 1)
     const int sk = ld_cluster_s32(cluster_addr(const_cast<int*>(skip), 0));
     cluster_sync();  // the leader's flag has been read before anyone may leave
     if (sk) return;  // an earlier kernel of this call failed; uniform over the pair
+    if (a.rowsA_dev) a.rowsA = min(*a.rowsA_dev, a.rowsA);  // written by an earlier kernel: same in both CTAs
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
         tmem_relinquish_pair();

@@ -268,8 +268,10 @@ __global__ void k_fill_dense(const uint16_t* __restrict__ h, int ldh, TwellView 
 // Slots of row r (a warp) from the up-projection epilogue's staging: the row's
 // column blocks are concatenated in block order (each block's entries are
 // already ascending), then padded.
+// With ov_pos (hybrid format), rows routed to the dense overflow block
+// (ov_pos[r] >= 0) are left empty here: padding only.
 __global__ void k_fill_staged_relu(const uint32_t* __restrict__ stage, const int32_t* __restrict__ stage_cnt, int NB,
-                                   int BN, TwellView tw, const int32_t* status)
+                                   int BN, TwellView tw, const int32_t* __restrict__ ov_pos, const int32_t* status)
 {
     const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -277,7 +279,8 @@ __global__ void k_fill_staged_relu(const uint32_t* __restrict__ stage, const int
     int Kt;
     const int64_t base = row_base(tw, r, &Kt);
     int pos = 0;
-    for (int nb0 = 0; nb0 < NB; nb0 += 32) {
+    const int nb_end = (ov_pos && ov_pos[r] >= 0) ? 0 : NB;
+    for (int nb0 = 0; nb0 < nb_end; nb0 += 32) {
         const int nb = nb0 + lane;
         const int c = nb < NB ? stage_cnt[(size_t)r * NB + nb] : 0;
         const int incl = warp_incl_scan(c, lane);
@@ -324,6 +327,86 @@ __global__ void k_fill_staged_gate(const uint2* __restrict__ stage, const int32_
         tw.idx[base + k] = -1;
         tw.val[base + k] = 0;
         gval[base + k] = 0.f;
+    }
+}
+
+// ------------------------------------------------- hybrid (ELL + dense) --
+//
+// "Sparser, Faster, Lighter Transformer Language Models", Resumo Técnico §2,
+// "Formato Híbrido para Treinamento": rows are partitioned dynamically; rows
+// within the ELL capacity stay in the compact format, rows with more nonzeros
+// (overflow) go to a dense backup matrix. Here: a row with nnz > C is an
+// overflow row. Its TwELL row is empty (nnz 0, so the TwELL kernels need no
+// change) and its whole hidden row is written densely to the next row of the
+// overflow block, rows in ascending order.
+
+// One block of 1024 threads: overflow flags (nnz[r] > C), their ascending
+// positions, the row list and count; nnz of overflow rows set to 0 so that the
+// tile layout that follows sizes the TwELL on the remaining rows only.
+__global__ void __launch_bounds__(1024) k_overflow_rows(TwellView tw, int C, int cap_rows, int32_t* __restrict__ ov_pos,
+                                                        int32_t* __restrict__ ov_rows, int32_t* __restrict__ n_rows,
+                                                        int32_t* status)
+{
+    __shared__ int s_warp[32];
+    __shared__ int s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (has_error(status)) return;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (int r0 = 0; r0 < tw.M; r0 += 1024) {
+        const int r = r0 + tid;
+        const bool in = r < tw.M;
+        const int n = in ? tw.nnz[r] : 0;
+        const int f = (in && n > C) ? 1 : 0;
+        const int incl = warp_incl_scan(f, lane);
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = s_warp[lane];
+            s_warp[lane] = warp_incl_scan(w, lane);
+        }
+        __syncthreads();
+        const int pos = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + incl - f;
+        if (in) {
+            ov_pos[r] = f ? pos : -1;
+            if (f) {
+                if (pos < cap_rows) ov_rows[pos] = r;
+                tw.nnz[r] = 0;
+            }
+        }
+        __syncthreads();
+        if (tid == 0) s_carry += s_warp[31];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        *n_rows = min(s_carry, cap_rows);
+        if (s_carry > cap_rows) set_error(status, TWELL_ERR_CAPACITY);
+    }
+}
+
+// Block i writes overflow row i: zeros over all F columns, then the row's
+// staged entries at their columns. F % 8 == 0 (16-byte rows of 8 bf16).
+__global__ void __launch_bounds__(256) k_overflow_dense(const uint32_t* __restrict__ stage,
+                                                        const int32_t* __restrict__ stage_cnt, int NB, int BN, int F,
+                                                        const int32_t* __restrict__ ov_rows,
+                                                        const int32_t* __restrict__ n_rows, uint16_t* __restrict__ dense,
+                                                        const int32_t* status)
+{
+    const int i = blockIdx.x;
+    if (has_error(status) || i >= *n_rows) return;
+    const int r = ov_rows[i];
+    uint16_t* drow = dense + (size_t)i * F;
+    for (int c = threadIdx.x * 8; c < F; c += blockDim.x * 8)
+        *reinterpret_cast<uint4*>(drow + c) = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int nb = warp; nb < NB; nb += nw) {
+        const int c = stage_cnt[(size_t)r * NB + nb];
+        const uint32_t* src = stage + ((size_t)r * NB + nb) * BN;
+        for (int e = lane; e < c; e += 32) {
+            const uint32_t w = src[e];
+            drow[nb * BN + (int)(w & 0xffffu)] = (uint16_t)(w >> 16);
+        }
     }
 }
 
@@ -1139,10 +1222,28 @@ cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, i
 }
 
 cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
-                                    const TwellView& tw, int32_t* status, cudaStream_t s)
+                                    const TwellView& tw, const int32_t* ov_pos, int32_t* status, cudaStream_t s)
 {
     count_launches(1);
-    k_fill_staged_relu<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(stage, stage_cnt, NB, BN, tw, status);
+    k_fill_staged_relu<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(stage, stage_cnt, NB, BN, tw, ov_pos, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_overflow_rows(const TwellView& tw, int C, int cap_rows, int32_t* ov_pos, int32_t* ov_rows,
+                                 int32_t* n_rows, int32_t* status, cudaStream_t s)
+{
+    count_launches(1);
+    k_overflow_rows<<<1, 1024, 0, s>>>(tw, C, cap_rows, ov_pos, ov_rows, n_rows, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_overflow_dense(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN, int F,
+                                  const int32_t* ov_rows, const int32_t* n_rows, int cap_rows, uint16_t* dense,
+                                  const int32_t* status, cudaStream_t s)
+{
+    if (cap_rows <= 0) return cudaSuccess;
+    count_launches(1);
+    k_overflow_dense<<<cap_rows, 256, 0, s>>>(stage, stage_cnt, NB, BN, F, ov_rows, n_rows, dense, status);
     return cudaGetLastError();
 }
 

@@ -17,18 +17,20 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_build", "libtwell.so")
 
-OP_PACK, OP_SPMM_DOWN, OP_FFN_FWD, OP_FFN_BWD, OP_GATED_FWD = 0, 1, 2, 3, 4
+OP_PACK, OP_SPMM_DOWN, OP_FFN_FWD, OP_FFN_BWD, OP_GATED_FWD, OP_HYBRID_FWD = 0, 1, 2, 3, 4, 5
 
 # Every symbol include/twell.h declares.
 EXPORTED_SYMBOLS = (
     "twell_status_string", "twell_buf_slots_bound", "twell_workspace_bytes", "twell_device_sm_count",
     "twell_pack", "twell_up_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd",
     "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
-    "twell_set_kernel_timer", "twell_gather_probe",
+    "twell_set_kernel_timer", "twell_gather_probe", "twell_hybrid_up_pack", "twell_hybrid_spmm_down",
+    "twell_hybrid_ffn_fwd",
 )
 
 # Call sites of twell_set_kernel_timer.
-SITE_NONE, SITE_UP_GEMM, SITE_SPMM_DOWN, SITE_SDDMM, SITE_DX, SITE_CSC, SITE_WGRAD, SITE_DECODE_TAIL = range(8)
+(SITE_NONE, SITE_UP_GEMM, SITE_SPMM_DOWN, SITE_SDDMM, SITE_DX, SITE_CSC, SITE_WGRAD, SITE_DECODE_TAIL,
+ SITE_OVERFLOW_GEMM) = range(9)
 
 # Size of the library-owned workspace behind twell_ffn_fwd_static_ws.
 STATIC_WS_BYTES = 32 * 1024 * 1024
@@ -47,9 +49,15 @@ class _TwellBuf(ctypes.Structure):
                 ("idx", ctypes.c_void_p), ("val", ctypes.c_void_p)]
 
 
+class _TwellOverflow(ctypes.Structure):
+    _fields_ = [("C", ctypes.c_int32), ("cap_rows", ctypes.c_int32), ("n_rows", ctypes.c_void_p),
+                ("rows", ctypes.c_void_p), ("dense", ctypes.c_void_p)]
+
+
 _lib = None
 P, I32, I64, SZ, F32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 BUFP = ctypes.POINTER(_TwellBuf)
+OVP = ctypes.POINTER(_TwellOverflow)
 
 
 def load_library(path: str | None = None):
@@ -86,6 +94,12 @@ def load_library(path: str | None = None):
     lib.twell_dense_ffn_fwd.argtypes = [P, P, P, P, I32, I32, I32, P, P, P, P]
     lib.twell_ffn_fwd_static_ws.restype = I32
     lib.twell_ffn_fwd_static_ws.argtypes = [P, P, P, P, P, I32, I32, I32, I32, BUFP, P, P, P]
+    lib.twell_hybrid_up_pack.restype = I32
+    lib.twell_hybrid_up_pack.argtypes = [P, P, P, I32, I32, I32, I32, BUFP, OVP, P, SZ, P, P]
+    lib.twell_hybrid_spmm_down.restype = I32
+    lib.twell_hybrid_spmm_down.argtypes = [BUFP, OVP, P, P, I32, P, P, P]
+    lib.twell_hybrid_ffn_fwd.restype = I32
+    lib.twell_hybrid_ffn_fwd.argtypes = [P, P, P, P, P, I32, I32, I32, I32, BUFP, OVP, P, P, SZ, P, P]
     lib.twell_gather_probe.restype = I32
     lib.twell_gather_probe.argtypes = [P, I32, I32, P, I32, I32, P, P]
     lib.twell_check.restype = I32
@@ -162,6 +176,23 @@ class TwellBuffers:
         return int(self.off[-1].item())
 
 
+class TwellOverflow:
+    """Dense overflow block of the hybrid format (allocated by torch) and its C struct:
+    rows with more than C nonzeros, at most cap_rows of them, each as a full hidden row."""
+
+    def __init__(self, F: int, C: int, cap_rows: int, device="cuda"):
+        self.F, self.C, self.cap_rows = F, int(C), int(cap_rows)
+        self.n_rows = torch.zeros(1, dtype=torch.int32, device=device)
+        self.rows = torch.empty(max(self.cap_rows, 1), dtype=torch.int32, device=device)
+        self.dense = torch.empty(max(self.cap_rows, 1) * F, dtype=torch.int16, device=device)  # bf16 bits
+        self.struct = _TwellOverflow(self.C, self.cap_rows, self.n_rows.data_ptr(), self.rows.data_ptr(),
+                                     self.dense.data_ptr())
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
 def twell_pack(h: torch.Tensor, T: int, out: TwellBuffers, status: torch.Tensor, stream=None):
     M, F = h.shape
     if not h.is_cuda or h.element_size() != 2 or h.stride(1) != 1:
@@ -222,6 +253,37 @@ def twell_ffn_fwd(x, W_up, W_gate, b, W_down, T: int, h_out: TwellBuffers, y, ws
         _ptr(W_down, "W_down", bytes_per_elem=2, numel=F * d), M, d, F, T, h_out.ref,
         _ptr(y, "y", bytes_per_elem=2, numel=M * d), _ptr(ws, "ws"), ws.numel() * ws.element_size(),
         _ptr(status, "status", bytes_per_elem=4), _stream(stream)), "twell_ffn_fwd")
+
+
+def twell_hybrid_up_pack(x, W_up, b, T: int, h_out: TwellBuffers, ov: TwellOverflow, ws, status, stream=None):
+    M, d = x.shape
+    F = W_up.shape[0]
+    _check(load_library().twell_hybrid_up_pack(
+        _ptr(x, "x", bytes_per_elem=2), _ptr(W_up, "W_up", bytes_per_elem=2, numel=F * d),
+        _ptr(b, "b", bytes_per_elem=4, numel=F), M, d, F, T, h_out.ref, ov.ref, _ptr(ws, "ws"),
+        ws.numel() * ws.element_size(), _ptr(status, "status", bytes_per_elem=4), _stream(stream)),
+        "twell_hybrid_up_pack")
+
+
+def twell_hybrid_spmm_down(h: TwellBuffers, ov: TwellOverflow, W_down, W_downT, y, status, stream=None):
+    d = W_down.shape[1]
+    _check(load_library().twell_hybrid_spmm_down(
+        h.ref, ov.ref, _ptr(W_down, "W_down", bytes_per_elem=2, numel=h.F * d),
+        _ptr(W_downT, "W_downT", bytes_per_elem=2, numel=h.F * d), d,
+        _ptr(y, "y", bytes_per_elem=2, numel=h.M * d), _ptr(status, "status", bytes_per_elem=4), _stream(stream)),
+        "twell_hybrid_spmm_down")
+
+
+def twell_hybrid_ffn_fwd(x, W_up, b, W_down, W_downT, T: int, h_out: TwellBuffers, ov: TwellOverflow, y, ws,
+                         status, stream=None):
+    M, d = x.shape
+    F = W_up.shape[0]
+    _check(load_library().twell_hybrid_ffn_fwd(
+        _ptr(x, "x", bytes_per_elem=2), _ptr(W_up, "W_up", bytes_per_elem=2, numel=F * d),
+        _ptr(b, "b", bytes_per_elem=4, numel=F), _ptr(W_down, "W_down", bytes_per_elem=2, numel=F * d),
+        _ptr(W_downT, "W_downT", bytes_per_elem=2, numel=F * d), M, d, F, T, h_out.ref, ov.ref,
+        _ptr(y, "y", bytes_per_elem=2, numel=M * d), _ptr(ws, "ws"), ws.numel() * ws.element_size(),
+        _ptr(status, "status", bytes_per_elem=4), _stream(stream)), "twell_hybrid_ffn_fwd")
 
 
 def twell_ffn_fwd_static_ws(x, W_up, W_gate, b, W_down, T: int, h_out: TwellBuffers, y, status, stream=None):

@@ -415,6 +415,66 @@ def decode_leg(tw, peaks, flush, stream, reps: int = 30):
     return out
 
 
+# ELL capacity of the hybrid format as a fraction of d_ff: a row is cheaper
+# dense than gathered once nnz * 2 d bytes at the gather rate (~18.6 TB/s)
+# exceed 2 F d FLOP at the dense GEMM's rate (~1.65 PFLOP/s), i.e. above
+# ~1.1 % of d_ff.
+HYBRID_C_FRAC = 0.0125
+
+
+def hybrid_leg(tw, flush, stream, reps: int = 5):
+    """The skewed sweep workloads (8192 tokens, d_model 4096, d_ff 16384, x rows
+    scaled by LogNormal(0, 1), gate biases for nominal 90 / 99 / 99.9 %
+    sparsity): forward time and memory of plain TwELL, of the hybrid
+    ELL + dense-overflow format (C = 1.25 % of d_ff) and of the dense layer."""
+    inp = syn.config_inputs("sweep90")  # the three differ only in the bias
+    M, d, F, T = inp.M, inp.d, inp.F, inp.T
+    x, Wu, Wd = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_down)
+    WdT = Wd.view(F, d).t().contiguous()
+    C = round(HYBRID_C_FRAC * F)
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def timed(fn):
+        evs = []
+        for i in range(reps + 2):
+            flush.fill_(i & 0xff)
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b2.record(stream)
+            if i >= 2:
+                evs.append((a, b2))
+        torch.cuda.synchronize()
+        if tw.twell_check(st) != 0:
+            raise RuntimeError(f"hybrid leg: device status {tw.twell_check(st)}")
+        return statistics.median(a.elapsed_time(b2) for a, b2 in evs)
+
+    out = {"C": C, "workload": "M=8192, d_model=4096, d_ff=16384, T=128, x rows x LogNormal(0,1)"}
+    for name in ("sweep90", "sweep99", "sweep999"):
+        b = torch.full((F,), float(syn.CONFIGS[name]["bias"]), dtype=torch.float32, device="cuda")
+        buf = tw.TwellBuffers(M, F, T, M * F)
+        ws = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_FWD, M, d, F, T, M * F), dtype=torch.uint8,
+                         device="cuda")
+        ms_tw = timed(lambda: tw.twell_ffn_fwd(x, Wu, None, b, Wd, T, buf, y, ws, st))
+        slots, nnz = buf.slots(), int(buf.nnz.sum().item())
+        del buf, ws
+        hb = tw.TwellBuffers(M, F, T, M * C)
+        ov = tw.TwellOverflow(F, C, M)
+        wsh = torch.empty(tw.twell_workspace_bytes(tw.OP_HYBRID_FWD, M, d, F, T, 0), dtype=torch.uint8,
+                          device="cuda")
+        ms_h = timed(lambda: tw.twell_hybrid_ffn_fwd(x, Wu, b, Wd, WdT, T, hb, ov, y, wsh, st))
+        n_ov, ell_slots = int(ov.n_rows.item()), hb.slots()
+        del hb, ov, wsh
+        hd = torch.empty(M, F, dtype=torch.int16, device="cuda")
+        ms_d = timed(lambda: tw.twell_dense_ffn_fwd(x, Wu, b, WdT, hd, y, st))
+        del hd
+        out[name] = {"density": nnz / (M * F), "twell_ms": ms_tw, "hybrid_ms": ms_h, "dense_ms": ms_d,
+                     "twell_MB": slots * 6 / 1e6, "hybrid_MB": (ell_slots * 6 + n_ov * F * 2) / 1e6,
+                     "overflow_rows": n_ov, "hybrid_vs_twell": ms_tw / ms_h, "hybrid_vs_dense": ms_d / ms_h}
+    return out
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import activation_sparse_transformer_tcgen05_gb300 as tw
     from activation_sparse_transformer_tcgen05_gb300 import build as tbuild
@@ -567,6 +627,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dense_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in dts[3:]) if dts else None
 
     decode = None if args.no_extras else decode_leg(tw, peaks, flush, stream)
+    hybrid = None if args.no_extras else hybrid_leg(tw, flush, stream)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.no_extras:
@@ -593,6 +654,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "stages": stages,
         "kernels": kernels,
         "dense_tcgen05_fwd_ms": dense_ms,
+        "hybrid": hybrid,
         "decode": decode,
         "wall_s_timed": t_wall,
     }

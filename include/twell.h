@@ -77,7 +77,7 @@ typedef struct twell_buf {
 
 /* Operation codes for twell_workspace_bytes. */
 enum { TWELL_OP_PACK = 0, TWELL_OP_SPMM_DOWN = 1, TWELL_OP_FFN_FWD = 2,
-       TWELL_OP_FFN_BWD = 3, TWELL_OP_GATED_FWD = 4 };
+       TWELL_OP_FFN_BWD = 3, TWELL_OP_GATED_FWD = 4, TWELL_OP_HYBRID_FWD = 5 };
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* twell_status_string(int status);
@@ -148,6 +148,57 @@ twell_status twell_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const uint16
                            const float* b, const uint16_t* W_down, int M, int d, int F, int T,
                            const twell_buf* h_out, uint16_t* y, void* ws, size_t ws_bytes,
                            int32_t* status, void* stream);
+
+/*
+ * Hybrid format (Resumo Técnico §2, "Formato Híbrido para Treinamento"): rows
+ * are partitioned dynamically; a row with more than C nonzeros is an overflow
+ * row and goes to a dense backup matrix, every other row stays in the TwELL.
+ * Overflow rows are empty rows of the TwELL (nnz 0), so every TwELL entry point
+ * applies to the TwELL part unchanged.
+ *   C         ELL capacity per row, >= 0
+ *   cap_rows  rows the dense block can hold, >= 0
+ *   n_rows    [1] int32 device, written: number of overflow rows
+ *   rows      [cap_rows] int32 device, written: overflow row ids, ascending
+ *   dense     [cap_rows, F] bf16 device, written: row i is the hidden row of
+ *             rows[i] (all F columns, zeros included)
+ * More than cap_rows overflow rows: *status = TWELL_ERR_CAPACITY and the first
+ * cap_rows are kept. All arrays are caller-owned.
+ */
+typedef struct {
+    int32_t C;
+    int32_t cap_rows;
+    int32_t* n_rows;
+    int32_t* rows;
+    uint16_t* dense;
+} twell_overflow;
+
+/*
+ * twell_hybrid_up_pack — ReLU up-projection (as twell_up_pack) packed into the
+ * hybrid format: h_out holds the rows with nnz <= ov->C, ov the others.
+ *   x [M, d] bf16; W_up [F, d] bf16; b [F] fp32; ws: at least
+ *   twell_workspace_bytes(TWELL_OP_HYBRID_FWD, M, d, F, T, 0) bytes,
+ *   256-byte aligned.
+ */
+twell_status twell_hybrid_up_pack(const uint16_t* x, const uint16_t* W_up, const float* b, int M, int d, int F,
+                                  int T, const twell_buf* h_out, const twell_overflow* ov, void* ws,
+                                  size_t ws_bytes, int32_t* status, void* stream);
+
+/*
+ * twell_hybrid_spmm_down — y = h W_down on the hybrid format: the TwELL rows by
+ * the sparse down-projection (twell_spmm_down), the overflow rows by the
+ * tcgen05 dense GEMM on ov->dense, its output rows placed by ov->rows.
+ *   W_down [F, d] bf16 (rows gathered by the TwELL part); W_downT [d, F] bf16,
+ *   the same matrix transposed (the dense GEMM's K-major operand); y [M, d]
+ *   bf16, every row written.
+ */
+twell_status twell_hybrid_spmm_down(const twell_buf* h, const twell_overflow* ov, const uint16_t* W_down,
+                                    const uint16_t* W_downT, int d, uint16_t* y, int32_t* status, void* stream);
+
+/* twell_hybrid_ffn_fwd — twell_hybrid_up_pack followed by twell_hybrid_spmm_down. */
+twell_status twell_hybrid_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const float* b, const uint16_t* W_down,
+                                  const uint16_t* W_downT, int M, int d, int F, int T, const twell_buf* h_out,
+                                  const twell_overflow* ov, uint16_t* y, void* ws, size_t ws_bytes,
+                                  int32_t* status, void* stream);
 
 /*
  * twell_ffn_bwd — backward of L = <dy, y> + l1_coef * sum |h| for the ReLU
@@ -224,9 +275,11 @@ twell_status twell_ffn_fwd_static_ws(const uint16_t* x, const uint16_t* W_up, co
  *   6 backward weight gradients
  *   7 gated decode tail (M <= 64: layout, gated up products and, in
  *     twell_ffn_fwd, the down-projection, in one launch)
+ *   8 dense GEMM of the hybrid format's overflow rows (twell_hybrid_spmm_down)
  */
 enum { TWELL_SITE_NONE = 0, TWELL_SITE_UP_GEMM = 1, TWELL_SITE_SPMM_DOWN = 2, TWELL_SITE_SDDMM = 3,
-       TWELL_SITE_DX = 4, TWELL_SITE_CSC = 5, TWELL_SITE_WGRAD = 6, TWELL_SITE_DECODE_TAIL = 7 };
+       TWELL_SITE_DX = 4, TWELL_SITE_CSC = 5, TWELL_SITE_WGRAD = 6, TWELL_SITE_DECODE_TAIL = 7,
+       TWELL_SITE_OVERFLOW_GEMM = 8 };
 twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end);
 
 /*

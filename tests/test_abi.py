@@ -70,7 +70,7 @@ def test_host_argument_errors_need_no_gpu(lib):
     fake = ctypes.c_void_p(256)  # never dereferenced: d % 8 != 0 is rejected first
     rc = lib.twell_gather_probe(fake, 8192, 2044, fake, 4096, 82, fake, None)
     assert rc == 1
-    assert lib.twell_set_kernel_timer(8, None, None) == 1  # no such call site
+    assert lib.twell_set_kernel_timer(9, None, None) == 1  # no such call site
 
 
 def test_ops_fail_loudly_without_library(tmp_path):
