@@ -48,7 +48,7 @@ cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, i
 // Slots from GEMM-epilogue staging. ReLU staging: uint32 (bf16 << 16 | local col);
 // gate staging: uint2 (global col, fp32 gate bits) and gate values go to gval[slot].
 // ov_pos (hybrid format, else null): rows with ov_pos[r] >= 0 are left empty.
-cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
+cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN, int stride,
                                     const TwellView& tw, const int32_t* ov_pos, int32_t* status, cudaStream_t s);
 // Hybrid format: overflow rows (nnz > C) in ascending order, nnz of those rows
 // set to 0 (run before launch_tile_layout), then their dense hidden rows.
@@ -65,7 +65,7 @@ bool small_fill_ok(int M, int NB);
 cudaError_t launch_layout_fill_small_gate(const uint2* stage, const int32_t* stage_cnt, int NB, int BM,
                                           const TwellView& tw, float* gval, int32_t* status, cudaStream_t s);
 cudaError_t launch_layout_fill_small_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
-                                          const TwellView& tw, int32_t* status, cudaStream_t s);
+                                          int stride, const TwellView& tw, int32_t* status, cudaStream_t s);
 
 // ---- Sparse products (twell_sparse.cu)
 // y[r,:] = sum_k v[r,k] * W[idx[r,k], :]; v is the TwELL's bf16 val (vals_f32 == nullptr)
@@ -110,7 +110,8 @@ struct GemmArgs {
     int rowsA, rowsB, K;   // A [rowsA, K], B [rowsB, K], both bf16 K-major
     const float* bias;     // TWELL_RELU: per B row; GATE_SWAP: per A row; DENSE: per B row or null
     int relu;              // DENSE only
-    uint32_t* stage;       // TWELL_RELU staging [rowsA, NB, BN]
+    uint32_t* stage;       // TWELL_RELU staging [rowsA, NB, stage_cap]
+    int stage_cap;         // TWELL_RELU: entries a (row, BN-column block) segment holds (<= BN)
     uint2* gstage;         // GATE_SWAP staging [rowsB, NB, 128]
     int32_t* stage_cnt;    // [rows, NB]
     int32_t* nnz;          // [rows], zeroed by the caller before the launch; null: not counted

@@ -44,6 +44,7 @@ struct Carver {
 
 constexpr int kReluBN = 256;  // column block of the ReLU GEMM epilogue
 constexpr int kGateBM = 128;  // hidden-unit block of the gate GEMM epilogue
+constexpr int kMinStageCap = 8;  // smallest ReLU staging capacity per (row, column block)
 
 struct FwdWs {
     int32_t* stage_cnt;
@@ -54,14 +55,15 @@ struct FwdWs {
     int32_t* ov_pos;   // hybrid: position of row r in the overflow block, or -1
 };
 
-size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out, bool hybrid = false)
+size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out, bool hybrid = false,
+                 int stage_cap = kReluBN)
 {
     Carver c{static_cast<char*>(ws)};
     FwdWs w{};
     if (!gated) {
         const size_t NB = (F + kReluBN - 1) / kReluBN;
         w.stage_cnt = c.take<int32_t>((size_t)M * NB);
-        w.stage = c.take<uint32_t>((size_t)M * NB * kReluBN);
+        w.stage = c.take<uint32_t>((size_t)M * NB * (size_t)stage_cap);
         if (hybrid) w.ov_pos = c.take<int32_t>((size_t)M);
     } else {
         const size_t NB = (F + kGateBM - 1) / kGateBM;
@@ -167,6 +169,24 @@ size_t twell_workspace_bytes(int op, int M, int d, int F, int T, int64_t cap_slo
     }
 }
 
+// Staging capacity per (row, 256-column block) a ReLU-forward workspace of
+// ws_bytes allows: the largest of 256, 128, ..., 8 that fits, or 0.
+static int relu_stage_cap(int M, int F, int64_t cap, size_t ws_bytes)
+{
+    for (int S = kReluBN; S >= kMinStageCap; S >>= 1)
+        if (carve_fwd(nullptr, false, M, F, cap, nullptr, false, S) <= ws_bytes) return S;
+    return 0;
+}
+
+size_t twell_fwd_workspace_bytes(int M, int d, int F, int T, int64_t cap_slots, int stage_cap)
+{
+    (void)d;
+    (void)T;
+    if (M <= 0 || F <= 0 || stage_cap < kMinStageCap || stage_cap > kReluBN || (stage_cap & (stage_cap - 1)) != 0)
+        return 0;
+    return carve_fwd(nullptr, false, M, F, cap_slots, nullptr, false, stage_cap);
+}
+
 int twell_device_sm_count(void) { return sm_count_current(); }
 
 twell_status twell_pack(const uint16_t* h, int M, int F, int ldh, int T, const twell_buf* out, int32_t* status,
@@ -216,8 +236,13 @@ twell_status up_pack_impl(const uint16_t* x, const uint16_t* W_up, const uint16_
     if (st != TWELL_OK) return st;
     const bool gated = W_gate != nullptr;
     if (gated && d > kMaxD) return TWELL_ERR_UNSUPPORTED;
-    const size_t need = carve_fwd(nullptr, gated, M, F, h_out->cap_slots, nullptr);
-    if (!ws || ws_bytes < need) return TWELL_ERR_WORKSPACE;
+    // ReLU: the epilogue staging holds as many entries per (row, 256-column
+    // block) as the workspace allows (the "predicted N_nz" capacity); gated:
+    // full blocks
+    const int stage_cap = gated ? kReluBN : relu_stage_cap(M, F, h_out->cap_slots, ws_bytes);
+    if (!ws || stage_cap == 0) return TWELL_ERR_WORKSPACE;
+    const size_t need = carve_fwd(nullptr, gated, M, F, h_out->cap_slots, nullptr, false, stage_cap);
+    if (ws_bytes < need) return TWELL_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;
     const int sms = sm_count_current();
     if (sms <= 0) return TWELL_ERR_CUDA;
@@ -225,7 +250,7 @@ twell_status up_pack_impl(const uint16_t* x, const uint16_t* W_up, const uint16_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const TwellView tw = view_of(h_out);
     FwdWs w;
-    carve_fwd(ws, gated, M, F, h_out->cap_slots, &w);
+    carve_fwd(ws, gated, M, F, h_out->cap_slots, &w, false, stage_cap);
     const bool tail = gated && decode_tail_ok(M, (F + kGateBM - 1) / kGateBM, tw.n_tiles);
     // the decode tail derives nnz from the staged counts; the other paths count into it
     cudaError_t e = tail ? cudaSuccess : cudaMemsetAsync(tw.nnz, 0, sizeof(int32_t) * (size_t)M, s);
@@ -239,15 +264,18 @@ twell_status up_pack_impl(const uint16_t* x, const uint16_t* W_up, const uint16_
         ga.rowsA = M;
         ga.rowsB = F;
         ga.stage = w.stage;
+        ga.stage_cap = stage_cap;
         ga.NB = (F + kReluBN - 1) / kReluBN;
         timer_begin(TWELL_SITE_UP_GEMM, s);
         if (e == cudaSuccess) e = launch_gemm(GEMM_TWELL_RELU, x, W_up, ga, sms, s);
         timer_end(TWELL_SITE_UP_GEMM, s);
         if (small_fill_ok(M, ga.NB)) {
-            if (e == cudaSuccess) e = launch_layout_fill_small_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, status, s);
+            if (e == cudaSuccess)
+                e = launch_layout_fill_small_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, stage_cap, tw, status, s);
         } else {
             if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
-            if (e == cudaSuccess) e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, nullptr, status, s);
+            if (e == cudaSuccess)
+                e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, stage_cap, tw, nullptr, status, s);
         }
     } else {
         ga.rowsA = F;
@@ -354,6 +382,7 @@ twell_status twell_hybrid_up_pack(const uint16_t* x, const uint16_t* W_up, const
     ga.rowsA = M;
     ga.rowsB = F;
     ga.stage = w.stage;
+    ga.stage_cap = kReluBN;  // overflow rows can be dense: full blocks
     ga.NB = (F + kReluBN - 1) / kReluBN;
     timer_begin(TWELL_SITE_UP_GEMM, s);
     if (e == cudaSuccess) e = launch_gemm(GEMM_TWELL_RELU, x, W_up, ga, sms, s);
@@ -361,7 +390,8 @@ twell_status twell_hybrid_up_pack(const uint16_t* x, const uint16_t* W_up, const
     if (e == cudaSuccess)
         e = launch_overflow_rows(tw, ov->C, ov->cap_rows, w.ov_pos, ov->rows, ov->n_rows, status, s);
     if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
-    if (e == cudaSuccess) e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, tw, w.ov_pos, status, s);
+    if (e == cudaSuccess)
+        e = launch_fill_staged_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, kReluBN, tw, w.ov_pos, status, s);
     if (e == cudaSuccess)
         e = launch_overflow_dense(w.stage, w.stage_cnt, ga.NB, kReluBN, F, ov->rows, ov->n_rows, ov->cap_rows,
                                   ov->dense, status, s);

@@ -70,7 +70,8 @@ __device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int nb, c
                                               const float* bias_sm)
 {
     const bool row_ok = row < a.rowsA;
-    uint32_t* st = a.stage + ((size_t)(row_ok ? row : 0) * a.NB + nb) * BN;
+    const int cap = a.stage_cap;
+    uint32_t* st = a.stage + ((size_t)(row_ok ? row : 0) * a.NB + nb) * cap;
     int cnt = 0;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
@@ -90,12 +91,18 @@ __device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int nb, c
                 const float p = __uint_as_float(v[c]) + bv[e];
                 const uint32_t hb = f32_to_bf16_bits(p);
                 const bool act = row_ok && p > 0.f && hb != 0u;
-                if (act) st[cnt] = (hb << 16) | (uint32_t)(ch * 32 + c);
+                if (act && cnt < cap) st[cnt] = (hb << 16) | (uint32_t)(ch * 32 + c);
                 cnt += act ? 1 : 0;
             }
         }
     }
     if (row_ok) {
+        // a segment with more nonzeros than the staging holds: the call fails
+        // with a capacity error; counts stay within what was staged
+        if (cnt > cap) {
+            set_error(a.status, TWELL_ERR_CAPACITY);
+            cnt = cap;
+        }
         a.stage_cnt[(size_t)row * a.NB + nb] = cnt;
         if (cnt) atomicAdd(&a.nnz[row], cnt);
     }

@@ -271,7 +271,8 @@ __global__ void k_fill_dense(const uint16_t* __restrict__ h, int ldh, TwellView 
 // With ov_pos (hybrid format), rows routed to the dense overflow block
 // (ov_pos[r] >= 0) are left empty here: padding only.
 __global__ void k_fill_staged_relu(const uint32_t* __restrict__ stage, const int32_t* __restrict__ stage_cnt, int NB,
-                                   int BN, TwellView tw, const int32_t* __restrict__ ov_pos, const int32_t* status)
+                                   int BN, int stride, TwellView tw, const int32_t* __restrict__ ov_pos,
+                                   const int32_t* status)
 {
     const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -285,7 +286,7 @@ __global__ void k_fill_staged_relu(const uint32_t* __restrict__ stage, const int
         const int c = nb < NB ? stage_cnt[(size_t)r * NB + nb] : 0;
         const int incl = warp_incl_scan(c, lane);
         const int64_t p = base + pos + (incl - c);
-        const uint32_t* src = stage + ((size_t)r * NB + nb) * BN;
+        const uint32_t* src = stage + ((size_t)r * NB + nb) * stride;
         for (int e = 0; e < c; ++e) {
             const uint32_t w = src[e];
             tw.idx[p + e] = nb * BN + (int)(w & 0xffffu);
@@ -421,7 +422,7 @@ constexpr int kSmallFillMax = 8192;
 template <typename Entry>
 __global__ void __launch_bounds__(1024) k_layout_fill_small(const Entry* __restrict__ stage,
                                                             const int32_t* __restrict__ stage_cnt, int NB, int BW,
-                                                            TwellView tw, float* gval, int32_t* status)
+                                                            int stride, TwellView tw, float* gval, int32_t* status)
 {
     __shared__ int s_cnt[kSmallFillMax];  // per (row, block): count, then exclusive prefix within the row
     __shared__ int s_nnz[1024];
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(1024) k_layout_fill_small(const Entry* __restr
         const int t = r / tw.T;
         const long long base = s_off[t] + (long long)(r - t * tw.T) * s_K[t] + s_cnt[i];
         const int c = stage_cnt[i];
-        const Entry* src = stage + (size_t)i * BW;
+        const Entry* src = stage + (size_t)i * stride;
         for (int e = 0; e < c; ++e) {
             const Entry w = src[e];
             if constexpr (sizeof(Entry) == 8) {
@@ -1221,11 +1222,12 @@ cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, i
     return cudaGetLastError();
 }
 
-cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
+cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN, int stride,
                                     const TwellView& tw, const int32_t* ov_pos, int32_t* status, cudaStream_t s)
 {
     count_launches(1);
-    k_fill_staged_relu<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(stage, stage_cnt, NB, BN, tw, ov_pos, status);
+    k_fill_staged_relu<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(stage, stage_cnt, NB, BN, stride, tw, ov_pos,
+                                                                     status);
     return cudaGetLastError();
 }
 
@@ -1382,16 +1384,16 @@ cudaError_t launch_layout_fill_small_gate(const uint2* stage, const int32_t* sta
 {
     count_launches(1);
     const int nblk = (tw.M * NB + 1023) / 1024;
-    k_layout_fill_small<uint2><<<nblk, 1024, 0, s>>>(stage, stage_cnt, NB, BM, tw, gval, status);
+    k_layout_fill_small<uint2><<<nblk, 1024, 0, s>>>(stage, stage_cnt, NB, BM, BM, tw, gval, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_layout_fill_small_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN,
-                                          const TwellView& tw, int32_t* status, cudaStream_t s)
+                                          int stride, const TwellView& tw, int32_t* status, cudaStream_t s)
 {
     count_launches(1);
     const int nblk = (tw.M * NB + 1023) / 1024;
-    k_layout_fill_small<uint32_t><<<nblk, 1024, 0, s>>>(stage, stage_cnt, NB, BN, tw, nullptr, status);
+    k_layout_fill_small<uint32_t><<<nblk, 1024, 0, s>>>(stage, stage_cnt, NB, BN, stride, tw, nullptr, status);
     return cudaGetLastError();
 }
 

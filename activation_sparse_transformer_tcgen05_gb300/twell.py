@@ -25,7 +25,7 @@ EXPORTED_SYMBOLS = (
     "twell_pack", "twell_up_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd",
     "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
     "twell_set_kernel_timer", "twell_gather_probe", "twell_hybrid_up_pack", "twell_hybrid_spmm_down",
-    "twell_hybrid_ffn_fwd",
+    "twell_hybrid_ffn_fwd", "twell_fwd_workspace_bytes",
 )
 
 # Call sites of twell_set_kernel_timer.
@@ -76,6 +76,8 @@ def load_library(path: str | None = None):
     lib.twell_buf_slots_bound.argtypes = [I32, I32, I32]
     lib.twell_workspace_bytes.restype = SZ
     lib.twell_workspace_bytes.argtypes = [I32, I32, I32, I32, I32, I64]
+    lib.twell_fwd_workspace_bytes.restype = SZ
+    lib.twell_fwd_workspace_bytes.argtypes = [I32, I32, I32, I32, I64, I32]
     lib.twell_device_sm_count.restype = I32
     lib.twell_pack.restype = I32
     lib.twell_pack.argtypes = [P, I32, I32, I32, I32, BUFP, P, P]
@@ -118,6 +120,11 @@ def twell_buf_slots_bound(M: int, F: int, T: int) -> int:
 
 def twell_workspace_bytes(op: int, M: int, d: int, F: int, T: int, cap_slots: int = 0) -> int:
     return int(load_library().twell_workspace_bytes(op, M, d, F, T, cap_slots))
+
+
+def twell_fwd_workspace_bytes(M: int, d: int, F: int, T: int, cap_slots: int, stage_cap: int) -> int:
+    """ReLU-forward workspace whose epilogue staging holds stage_cap entries per (row, 256-column block)."""
+    return int(load_library().twell_fwd_workspace_bytes(M, d, F, T, cap_slots, stage_cap))
 
 
 def twell_device_sm_count() -> int:

@@ -40,6 +40,7 @@ import synthetic as syn  # noqa: E402
 METRIC = "sparse-FFN tokens/s fwd & fwd+bwd at 99% sparsity; % of HBM/tensor roofline"
 UNIT = "tokens/s"
 CONFIG_NAME = "inference"
+STAGE_CAP = 32
 WORKLOAD = ("inference FFN layer: M=4096 tokens, d_model=2048, d_ff=8192, bf16, ReLU, bias=-2.33 "
             "(~99% sparse), TwELL tile=128 rows, fp32 accumulation; step = fwd + bwd (dy~N(0,1), L1=1e-4)")
 L1 = 1e-4
@@ -196,7 +197,9 @@ class Layer:
         self.cap = M * F
         self.buf = tw.TwellBuffers(M, F, T, self.cap)
         self.y = torch.empty(M, d, dtype=torch.int16, device="cuda")
-        self.ws_f = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_FWD, M, d, F, T, self.cap), dtype=torch.uint8,
+        # epilogue staging of 32 entries per (row, 256-column block): ~13x the
+        # mean count at 1 % density (the full 256 would be as large as an fp32 h)
+        self.ws_f = torch.empty(tw.twell_fwd_workspace_bytes(M, d, F, T, self.cap, STAGE_CAP), dtype=torch.uint8,
                                 device="cuda")
         self.ws_b = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, self.cap), dtype=torch.uint8,
                                 device="cuda")
@@ -218,6 +221,83 @@ class Layer:
 
 
 SITES = {1: "up_gemm", 2: "spmm_down", 3: "sddmm", 4: "dx", 5: "csc", 6: "wgrad"}
+
+
+class PowerSampler:
+    """nvidia-smi board power samples (50 ms) with their timestamps."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=timestamp,power.draw", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        """[(unix time, watts)]"""
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        samples = []
+        for line in out.strip().splitlines():
+            parts = [q.strip() for q in line.split(",")]
+            if len(parts) < 2:
+                continue
+            try:
+                t = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                samples.append((t + frac, float(parts[1])))
+            except ValueError:
+                continue
+        return samples
+
+
+def energy_leg(tw, local_rank: int, runs: dict, tokens: int, seconds: float = 2.0):
+    """Energy per token of back-to-back calls of each callable in `runs`
+    (board power from nvidia-smi, averaged over the samples inside the loop)."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name, fn in runs.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(5):
+            fn()
+        b2.record(stream)
+        torch.cuda.synchronize()
+        per = a.elapsed_time(b2) / 5 / 1000.0
+        n = max(10, int(seconds / per))
+        ps = PowerSampler(local_rank)
+        ps.start()
+        time.sleep(0.5)
+        t0 = time.time()
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b2.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        samples = [w for t, w in ps.stop() if t0 + 0.1 <= t <= t1]
+        if not samples:
+            out[name] = None
+            continue
+        s_run = a.elapsed_time(b2) / 1000.0
+        watts = statistics.mean(samples)
+        out[name] = {"watts": watts, "ms_per_call": s_run / n * 1000.0, "mJ_per_call": watts * s_run / n * 1000.0,
+                     "uJ_per_token": watts * s_run / (n * tokens) * 1e6, "samples": len(samples), "calls": n}
+    return out
 
 
 def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:
@@ -626,6 +706,24 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     dense_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in dts[3:]) if dts else None
 
+    # ---- energy per token and memory, sparse against dense (forward; and the sparse training step)
+    energy, memory = None, None
+    if not args.no_extras:
+        energy = energy_leg(tw, local_rank, {
+            "twell_fwd": lambda: tw.twell_ffn_fwd(L.x, L.Wu, None, L.b, L.Wd, inp.T, L.buf, L.y, L.ws_f, L.st),
+            "dense_fwd": lambda: tw.twell_dense_ffn_fwd(L.x, L.Wu, L.b, WdT, hd, L.y, L.st),
+            "twell_fwd_bwd": lambda: (L.up(), L.down(), L.bwd()),
+        }, inp.M)
+        if energy.get("twell_fwd") and energy.get("dense_fwd"):
+            energy["dense_over_twell_fwd"] = energy["dense_fwd"]["uJ_per_token"] / energy["twell_fwd"]["uJ_per_token"]
+        memory = {
+            "saved_for_backward_MB": {"twell": (slots * 6 + inp.M * 4 + (inp.M // inp.T + 2) * 12) / 1e6,
+                                      "dense_h_bf16": inp.M * inp.F * 2 / 1e6},
+            "forward_workspace_MB": {"twell": L.ws_f.numel() / 1e6, "twell_stage_cap": STAGE_CAP,
+                                     "dense_h_bf16": inp.M * inp.F * 2 / 1e6},
+            "backward_workspace_MB": {"twell_at_actual_slots": tw.twell_workspace_bytes(
+                tw.OP_FFN_BWD, inp.M, inp.d, inp.F, inp.T, slots) / 1e6},
+        }
     decode = None if args.no_extras else decode_leg(tw, peaks, flush, stream)
     hybrid = None if args.no_extras else hybrid_leg(tw, flush, stream)
 
@@ -655,6 +753,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "kernels": kernels,
         "dense_tcgen05_fwd_ms": dense_ms,
         "hybrid": hybrid,
+        "energy": energy,
+        "memory": memory,
         "decode": decode,
         "wall_s_timed": t_wall,
     }

@@ -91,6 +91,18 @@ int64_t twell_buf_slots_bound(int M, int F, int T);
  * none is needed. */
 size_t twell_workspace_bytes(int op, int M, int d, int F, int T, int64_t cap_slots);
 
+/*
+ * twell_fwd_workspace_bytes — workspace of the ReLU forward (twell_up_pack /
+ * twell_ffn_fwd without a gate) whose up-projection epilogue stages at most
+ * stage_cap nonzeros per (row, 256-column block): the capacity the method
+ * predicts for N_nz (Resumo Técnico §2, "Formato Híbrido para Treinamento").
+ * stage_cap is a power of two in [8, 256]; 256 never overflows and equals
+ * twell_workspace_bytes(TWELL_OP_FFN_FWD, ...). The forward uses the largest
+ * capacity its ws_bytes allows; a block with more nonzeros than that makes the
+ * call report TWELL_ERR_CAPACITY. Returns 0 for invalid arguments.
+ */
+size_t twell_fwd_workspace_bytes(int M, int d, int F, int T, int64_t cap_slots, int stage_cap);
+
 /* Number of streaming multiprocessors the library sizes its grids for. */
 int twell_device_sm_count(void);
 

@@ -407,3 +407,33 @@ def test_gather_probe_reads_the_named_rows():
             c = words[idx[r], g * 128:min((g + 1) * 128, d // 2)]
             want[r * G + g] = np.bitwise_xor.reduce(c.reshape(-1)) & 0x007fffff
     np.testing.assert_array_equal(got, want)
+
+
+def _fwd_with_stage_cap(inp, stage_cap):
+    M, d, F, T = inp.M, inp.d, inp.F, inp.T
+    buf = tw.TwellBuffers(M, F, T, M * F)
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    ws = torch.empty(tw.twell_fwd_workspace_bytes(M, d, F, T, M * F, stage_cap), dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    tw.twell_ffn_fwd(dev_bf16(inp.x), dev_bf16(inp.W_up), None, dev_f32(inp.b), dev_bf16(inp.W_down), T, buf, y,
+                     ws, st)
+    return buf, y, st
+
+
+def test_fwd_small_staging_gives_the_same_twell():
+    # ~1 % active: at most a handful of nonzeros per (row, 256-column block), so
+    # a 16-entry staging segment never fills and the result is the full one's
+    inp = syn.ffn_inputs(520, 256, 2056, 64, -2.33, seed=8)
+    b16, y16, st16 = _fwd_with_stage_cap(inp, 16)
+    b256, y256, st256 = _fwd_with_stage_cap(inp, 256)
+    _status_ok(st16)
+    _status_ok(st256)
+    assert_twell_identical(twell_to_host(b16), twell_to_host(b256))
+    np.testing.assert_array_equal(host_bf16_bits(y16), host_bf16_bits(y256))
+
+
+def test_fwd_staging_overflow_is_reported():
+    # half the units active: ~128 per block, more than an 8-entry segment holds
+    inp = syn.ffn_inputs(300, 128, 1024, 32, 0.0, seed=9)
+    _, _, st = _fwd_with_stage_cap(inp, 8)
+    assert tw.twell_check(st) == 4  # TWELL_ERR_CAPACITY
