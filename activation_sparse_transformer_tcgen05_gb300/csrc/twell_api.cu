@@ -44,7 +44,6 @@ struct Carver {
 
 constexpr int kReluBN = 256;  // column block of the ReLU GEMM epilogue
 constexpr int kGateBM = 128;  // hidden-unit block of the gate GEMM epilogue
-constexpr int kMinStageCap = 8;  // smallest ReLU staging capacity per (row, column block)
 
 struct FwdWs {
     int32_t* stage_cnt;
@@ -63,7 +62,8 @@ size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out, bo
     if (!gated) {
         const size_t NB = (F + kReluBN - 1) / kReluBN;
         w.stage_cnt = c.take<int32_t>((size_t)M * NB);
-        w.stage = c.take<uint32_t>((size_t)M * NB * (size_t)stage_cap);
+        // + slack: a segment that overflows writes up to BN - cap words past its end
+        w.stage = c.take<uint32_t>((size_t)M * NB * (size_t)stage_cap + (size_t)(kReluBN - stage_cap));
         if (hybrid) w.ov_pos = c.take<int32_t>((size_t)M);
     } else {
         const size_t NB = (F + kGateBM - 1) / kGateBM;
@@ -169,11 +169,14 @@ size_t twell_workspace_bytes(int op, int M, int d, int F, int T, int64_t cap_slo
     }
 }
 
-// Staging capacity per (row, 256-column block) a ReLU-forward workspace of
-// ws_bytes allows: the largest of 256, 128, ..., 8 that fits, or 0.
+// Staging capacities per (row, 256-column block) the ReLU epilogue is built
+// for, largest first.
+constexpr int kStageCaps[] = {256, 64, 32};
+
+// The largest staging capacity a ReLU-forward workspace of ws_bytes allows, or 0.
 static int relu_stage_cap(int M, int F, int64_t cap, size_t ws_bytes)
 {
-    for (int S = kReluBN; S >= kMinStageCap; S >>= 1)
+    for (int S : kStageCaps)
         if (carve_fwd(nullptr, false, M, F, cap, nullptr, false, S) <= ws_bytes) return S;
     return 0;
 }
@@ -182,8 +185,9 @@ size_t twell_fwd_workspace_bytes(int M, int d, int F, int T, int64_t cap_slots, 
 {
     (void)d;
     (void)T;
-    if (M <= 0 || F <= 0 || stage_cap < kMinStageCap || stage_cap > kReluBN || (stage_cap & (stage_cap - 1)) != 0)
-        return 0;
+    bool ok = false;
+    for (int S : kStageCaps) ok = ok || S == stage_cap;
+    if (M <= 0 || F <= 0 || !ok) return 0;
     return carve_fwd(nullptr, false, M, F, cap_slots, nullptr, false, stage_cap);
 }
 

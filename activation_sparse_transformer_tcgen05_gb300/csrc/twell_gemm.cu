@@ -64,14 +64,15 @@ __device__ __forceinline__ void fail(int32_t* status, volatile int* abort_flag)
 
 // TwELL epilogue of one accumulator row (one thread): bias, ReLU, bf16
 // rounding, and the row's nonzeros of this BN-column block appended to its
-// staging segment as (bf16 << 16 | column within the block), ascending.
-template <int BN>
-__device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int nb, const GemmArgs& a,
+// staging segment of CAP words as (bf16 << 16 | column within the block),
+// ascending. CAP is a compile-time constant: a run-time segment stride made
+// this epilogue slow enough to hold back the MMAs.
+template <int BN, int CAP>
+__device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int rowsA, int nb, const GemmArgs& a,
                                               const float* bias_sm)
 {
-    const bool row_ok = row < a.rowsA;
-    const int cap = a.stage_cap;
-    uint32_t* st = a.stage + ((size_t)(row_ok ? row : 0) * a.NB + nb) * cap;
+    const bool row_ok = row < rowsA;
+    uint32_t* st = a.stage + ((size_t)(row_ok ? row : 0) * a.NB + nb) * CAP;
     int cnt = 0;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
@@ -91,7 +92,10 @@ __device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int nb, c
                 const float p = __uint_as_float(v[c]) + bv[e];
                 const uint32_t hb = f32_to_bf16_bits(p);
                 const bool act = row_ok && p > 0.f && hb != 0u;
-                if (act && cnt < cap) st[cnt] = (hb << 16) | (uint32_t)(ch * 32 + c);
+                // no capacity test per column: a segment that overflows spills
+                // into the next one (the workspace has BN - cap words of slack
+                // after the last), and the call then fails with a capacity error
+                if (act) st[cnt] = (hb << 16) | (uint32_t)(ch * 32 + c);
                 cnt += act ? 1 : 0;
             }
         }
@@ -99,9 +103,9 @@ __device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int nb, c
     if (row_ok) {
         // a segment with more nonzeros than the staging holds: the call fails
         // with a capacity error; counts stay within what was staged
-        if (cnt > cap) {
+        if (cnt > CAP) {
             set_error(a.status, TWELL_ERR_CAPACITY);
-            cnt = cap;
+            cnt = CAP;
         }
         a.stage_cnt[(size_t)row * a.NB + nb] = cnt;
         if (cnt) atomicAdd(&a.nnz[row], cnt);
@@ -110,10 +114,10 @@ __device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int nb, c
 
 // Dense epilogue of one accumulator row: bias, optional ReLU, bf16 stores.
 template <int BN>
-__device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int nb, const GemmArgs& a,
+__device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int rowsA, int nb, const GemmArgs& a,
                                               const float* bias_sm)
 {
-    const bool row_ok = row < a.rowsA;
+    const bool row_ok = row < rowsA;
     const int orow = (row_ok && a.row_map) ? a.row_map[row] : row;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
@@ -142,11 +146,10 @@ __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int nb, c
     }
 }
 
-template <int BN, int MODE, int STAGES>
+template <int BN, int MODE, int STAGES, int CAP = BN>
 __global__ void __launch_bounds__(192, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs args, int tok0)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a, int tok0)
 {
-    GemmArgs a = args;
     using L = Layout<BN, STAGES>;
     constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
     extern __shared__ uint8_t smem_raw[];
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     if (*skip) return;  // an earlier kernel of this call failed; uniform over the block
     if (a.zero_word && blockIdx.x == 0 && threadIdx.x == 0) *a.zero_word = 0;
-    if (a.rowsA_dev) a.rowsA = min(*a.rowsA_dev, a.rowsA);  // written by an earlier kernel
+    const int rowsA = a.rowsA_dev ? min(*a.rowsA_dev, a.rowsA) : a.rowsA;  // written by an earlier kernel
     if (warp == 1) {
         tmem_alloc(tmem_slot, L::TMEM_COLS);
         tmem_relinquish();
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_m = (a.rowsA + BM - 1) / BM;
+    const int num_m = (rowsA + BM - 1) / BM;
     const int num_n = (a.rowsB + BN - 1) / BN;
     const int num_kb = (a.K + BK - 1) / BK;
     const int num_tiles = num_m * num_n;
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
 
             if constexpr (MODE == GEMM_TWELL_RELU) {
-                epi_twell_row<BN>(tbase, mb * BM + 32 * q + lane, nb, a, bias_sm);
+                epi_twell_row<BN, CAP>(tbase, mb * BM + 32 * q + lane, rowsA, nb, a, bias_sm);
             } else if constexpr (MODE == GEMM_GATE_SWAP) {
                 const int j = mb * BM + 32 * q + lane;  // hidden unit
                 const bool j_ok = j < a.rowsA;
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             } else {  // GEMM_DENSE
-                epi_dense_row<BN>(tbase, mb * BM + 32 * q + lane, nb, a, bias_sm);
+                epi_dense_row<BN>(tbase, mb * BM + 32 * q + lane, rowsA, nb, a, bias_sm);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -408,11 +411,10 @@ struct PairLayout {
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
 };
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int CAP = PAIR_N>
 __global__ void __launch_bounds__(192, 1)
-    k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs args)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a)
 {
-    GemmArgs a = args;
     static_assert(MODE == GEMM_TWELL_RELU || MODE == GEMM_DENSE, "row-wise epilogues only");
     using L = PairLayout<STAGES>;
     constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, PAIR_N);
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(192, 1)
     const int sk = ld_cluster_s32(cluster_addr(const_cast<int*>(skip), 0));
     cluster_sync();  // the leader's flag has been read before anyone may leave
     if (sk) return;  // an earlier kernel of this call failed; uniform over the pair
-    if (a.rowsA_dev) a.rowsA = min(*a.rowsA_dev, a.rowsA);  // written by an earlier kernel: same in both CTAs
+    const int rowsA = a.rowsA_dev ? min(*a.rowsA_dev, a.rowsA) : a.rowsA;  // same in both CTAs
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
         tmem_relinquish_pair();
@@ -468,7 +470,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_m = (a.rowsA + PAIR_M - 1) / PAIR_M;
+    const int num_m = (rowsA + PAIR_M - 1) / PAIR_M;
     const int num_n = (a.rowsB + PAIR_N - 1) / PAIR_N;
     const int num_kb = (a.K + BK - 1) / BK;
     const int num_tiles = num_m * num_n;
@@ -578,9 +580,9 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * PAIR_N);
             const int row = mb * PAIR_M + (int)rank * HALF + 32 * q + lane;
             if constexpr (MODE == GEMM_TWELL_RELU)
-                epi_twell_row<PAIR_N>(tbase, row, nb, a, bias_sm);
+                epi_twell_row<PAIR_N, CAP>(tbase, row, rowsA, nb, a, bias_sm);
             else
-                epi_dense_row<PAIR_N>(tbase, row, nb, a, bias_sm);
+                epi_dense_row<PAIR_N>(tbase, row, rowsA, nb, a, bias_sm);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
@@ -635,13 +637,13 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, int STAGES>
+template <int BN, int MODE, int STAGES, int CAP = BN>
 cudaError_t run(const uint16_t* A, const uint16_t* B, const GemmArgs& a, int tok0, int sm_count, cudaStream_t s)
 {
     using L = Layout<BN, STAGES>;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, a.rowsA, a.K, BM) || !make_map(&mb, B, a.rowsB, a.K, BN)) return cudaErrorInvalidValue;
-    auto kern = k_gemm_tc<BN, MODE, STAGES>;
+    auto kern = k_gemm_tc<BN, MODE, STAGES, CAP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e != cudaSuccess) return e;
     const int tiles = ((a.rowsA + BM - 1) / BM) * ((a.rowsB + BN - 1) / BN);
@@ -652,7 +654,7 @@ cudaError_t run(const uint16_t* A, const uint16_t* B, const GemmArgs& a, int tok
 }
 
 // Clusters of two that can be resident at once for this kernel (0 = none).
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int CAP>
 int pair_capacity(cudaLaunchConfig_t cfg)
 {
     static int cached[64] = {0};
@@ -661,7 +663,7 @@ int pair_capacity(cudaLaunchConfig_t cfg)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (!known[dev]) {
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<MODE, STAGES>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<MODE, STAGES, CAP>, &cfg) != cudaSuccess) {
             (void)cudaGetLastError();
             n = 0;
         }
@@ -673,12 +675,12 @@ int pair_capacity(cudaLaunchConfig_t cfg)
 
 // Launches the pair kernel; *launched = false (and nothing enqueued) when no
 // cluster of two fits, so the caller can take the single-CTA kernel.
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int CAP = PAIR_N>
 cudaError_t run_pair(const uint16_t* A, const uint16_t* B, const GemmArgs& a, cudaStream_t s, bool* launched)
 {
     using L = PairLayout<STAGES>;
     *launched = false;
-    auto kern = k_gemm_pair<MODE, STAGES>;
+    auto kern = k_gemm_pair<MODE, STAGES, CAP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -693,7 +695,7 @@ cudaError_t run_pair(const uint16_t* A, const uint16_t* B, const GemmArgs& a, cu
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int cap = pair_capacity<MODE, STAGES>(cfg);
+    const int cap = pair_capacity<MODE, STAGES, CAP>(cfg);
     if (cap <= 0) return cudaSuccess;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, a.rowsA, a.K, HALF) || !make_map(&mb, B, a.rowsB, a.K, HALF)) return cudaErrorInvalidValue;
@@ -702,6 +704,20 @@ cudaError_t run_pair(const uint16_t* A, const uint16_t* B, const GemmArgs& a, cu
     count_launches(1);
     *launched = true;
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, a);
+}
+
+// Row-wise epilogues: 256 x 256 tiles on CTA pairs when there are more than
+// 128 rows, else (or without room for a cluster of two) 128 x 256 tiles on
+// single CTAs.
+template <int MODE, int CAP>
+cudaError_t launch_row_wise(const uint16_t* A, const uint16_t* B, const GemmArgs& a, int sm_count, cudaStream_t s)
+{
+    if (a.rowsA > HALF) {
+        bool launched = false;
+        const cudaError_t e = run_pair<MODE, 6, CAP>(A, B, a, s, &launched);
+        if (e != cudaSuccess || launched) return e;
+    }
+    return run<256, MODE, 4, CAP>(A, B, a, 0, sm_count, s);
 }
 
 }  // namespace
@@ -717,19 +733,15 @@ cudaError_t launch_gemm(int mode, const uint16_t* A, const uint16_t* B, const Ge
 {
     switch (mode) {
         case GEMM_TWELL_RELU:
-        case GEMM_DENSE: {
-            // Row-wise epilogues: 256 x 256 tiles on CTA pairs when there are
-            // more than 128 rows, else (or without room for a cluster of
-            // two) 128 x 256 tiles on single CTAs.
-            if (a.rowsA > HALF) {
-                bool launched = false;
-                const cudaError_t e = mode == GEMM_TWELL_RELU ? run_pair<GEMM_TWELL_RELU, 6>(A, B, a, s, &launched)
-                                                              : run_pair<GEMM_DENSE, 6>(A, B, a, s, &launched);
-                if (e != cudaSuccess || launched) return e;
+            // Staging segments of 256, 64 or 32 entries (compile-time strides).
+            switch (a.stage_cap) {
+                case 256: return launch_row_wise<GEMM_TWELL_RELU, 256>(A, B, a, sm_count, s);
+                case 64: return launch_row_wise<GEMM_TWELL_RELU, 64>(A, B, a, sm_count, s);
+                case 32: return launch_row_wise<GEMM_TWELL_RELU, 32>(A, B, a, sm_count, s);
+                default: return cudaErrorInvalidValue;
             }
-            return mode == GEMM_TWELL_RELU ? run<256, GEMM_TWELL_RELU, 4>(A, B, a, 0, sm_count, s)
-                                           : run<256, GEMM_DENSE, 4>(A, B, a, 0, sm_count, s);
-        }
+        case GEMM_DENSE:
+            return launch_row_wise<GEMM_DENSE, 256>(A, B, a, sm_count, s);
         case GEMM_GATE_SWAP: {
             // B = x: token chunks of at most 64 rows, each a separate launch.
             const int bn = gemm_block_n(mode, a.rowsB);

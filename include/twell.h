@@ -96,10 +96,11 @@ size_t twell_workspace_bytes(int op, int M, int d, int F, int T, int64_t cap_slo
  * twell_ffn_fwd without a gate) whose up-projection epilogue stages at most
  * stage_cap nonzeros per (row, 256-column block): the capacity the method
  * predicts for N_nz (Resumo Técnico §2, "Formato Híbrido para Treinamento").
- * stage_cap is a power of two in [8, 256]; 256 never overflows and equals
- * twell_workspace_bytes(TWELL_OP_FFN_FWD, ...). The forward uses the largest
- * capacity its ws_bytes allows; a block with more nonzeros than that makes the
- * call report TWELL_ERR_CAPACITY. Returns 0 for invalid arguments.
+ * stage_cap is 256, 64 or 32 (the capacities the epilogue is compiled for);
+ * 256 never overflows and equals twell_workspace_bytes(TWELL_OP_FFN_FWD, ...).
+ * The forward uses the largest of them its ws_bytes allows; a block with more
+ * nonzeros than that makes the call report TWELL_ERR_CAPACITY. Returns 0 for
+ * invalid arguments.
  */
 size_t twell_fwd_workspace_bytes(int M, int d, int F, int T, int64_t cap_slots, int stage_cap);
 

@@ -420,20 +420,22 @@ def _fwd_with_stage_cap(inp, stage_cap):
     return buf, y, st
 
 
-def test_fwd_small_staging_gives_the_same_twell():
+@pytest.mark.parametrize("M", [520, 100])  # CTA-pair GEMM; single-CTA GEMM
+def test_fwd_small_staging_gives_the_same_twell(M):
     # ~1 % active: at most a handful of nonzeros per (row, 256-column block), so
-    # a 16-entry staging segment never fills and the result is the full one's
-    inp = syn.ffn_inputs(520, 256, 2056, 64, -2.33, seed=8)
-    b16, y16, st16 = _fwd_with_stage_cap(inp, 16)
+    # a 32- or 64-entry staging segment never fills and the result is the full one's
+    inp = syn.ffn_inputs(M, 256, 2056, 64, -2.33, seed=8)
     b256, y256, st256 = _fwd_with_stage_cap(inp, 256)
-    _status_ok(st16)
     _status_ok(st256)
-    assert_twell_identical(twell_to_host(b16), twell_to_host(b256))
-    np.testing.assert_array_equal(host_bf16_bits(y16), host_bf16_bits(y256))
+    for cap in (64, 32):
+        b, y, st = _fwd_with_stage_cap(inp, cap)
+        _status_ok(st)
+        assert_twell_identical(twell_to_host(b), twell_to_host(b256))
+        np.testing.assert_array_equal(host_bf16_bits(y), host_bf16_bits(y256))
 
 
 def test_fwd_staging_overflow_is_reported():
-    # half the units active: ~128 per block, more than an 8-entry segment holds
+    # half the units active: ~128 per block, more than a 32-entry segment holds
     inp = syn.ffn_inputs(300, 128, 1024, 32, 0.0, seed=9)
-    _, _, st = _fwd_with_stage_cap(inp, 8)
+    _, _, st = _fwd_with_stage_cap(inp, 32)
     assert tw.twell_check(st) == 4  # TWELL_ERR_CAPACITY
