@@ -325,6 +325,12 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mas
         : "memory");
 }
 
+// Asks for the 128-byte line at p to be brought into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Named barrier among `nthreads` threads (whole warps) of the block.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
 {

@@ -289,6 +289,10 @@ twell_status up_pack_impl(const uint16_t* x, const uint16_t* W_up, const uint16_
         if (tail) {
             ga.nnz = nullptr;
             ga.zero_word = w.counter;
+            // the tail gathers the active units' W_up (and W_down) rows next
+            ga.pf0 = W_up;
+            ga.pf1 = W_down ? W_down : W_up;
+            ga.pf_row_bytes = 2 * d;
         }
         timer_begin(TWELL_SITE_UP_GEMM, s);
         if (e == cudaSuccess) e = launch_gemm(GEMM_GATE_SWAP, W_gate, x, ga, sms, s);

@@ -322,12 +322,27 @@ __global__ void __launch_bounds__(192, 1)
                         tmem_ld32_wait(tbase + ch * 32, v32);
                     }
                 }
+                bool any = false;
 #pragma unroll
                 for (int t = 0; t < BN; ++t) {
                     if (t < ntok) {
                         const bool act = j_ok && (__uint_as_float(v[t]) + bj > 0.f);
+                        any |= act;
                         const uint32_t m = __ballot_sync(0xffffffffu, act);
                         if (lane == 0) s_mask[t * 4 + q] = m;
+                    }
+                }
+                if (a.pf_row_bytes > 0) {
+                    // the next kernel reads the W_up and W_down rows of every
+                    // active unit: start pulling them into L2 now, one warp per row
+                    uint32_t units = __ballot_sync(0xffffffffu, any);
+                    while (units) {
+                        const int jj = mb * BM + 32 * q + __ffs(units) - 1;
+                        units &= units - 1;
+                        for (int off = lane * 128; off < a.pf_row_bytes; off += 32 * 128) {
+                            prefetch_l2(reinterpret_cast<const char*>(a.pf0) + (size_t)jj * a.pf_row_bytes + off);
+                            prefetch_l2(reinterpret_cast<const char*>(a.pf1) + (size_t)jj * a.pf_row_bytes + off);
+                        }
                     }
                 }
                 named_bar_sync(1, kEpiThreads);
