@@ -1,11 +1,11 @@
 // twell_gemm.cu — persistent tcgen05 GEMM with a TwELL-emitting epilogue.
 //
 // D = A B^T with A [rowsA, K] and B [rowsB, K] bf16, both K-major, fp32
-// accumulation in tensor memory. The pages build TwELL "directly in the
-// epilogue of highly optimised dense matmul kernels", with no separate
-// conversion kernel and no synchronisation between CTAs ("Sparser, Faster,
-// Lighter Transformer Language Models", Resumo Técnico §2, "Formato de Dados
-// TwELL"). Here each CTA compacts its own 128 x BN output tile independently:
+// accumulation in tensor memory. The method writes TwELL from the epilogue of
+// the dense matmul that computes the activations, so that neither a separate
+// conversion kernel nor synchronisation between CTAs is needed ("Sparser,
+// Faster, Lighter Transformer Language Models", Resumo Técnico §2, "Formato de
+// Dados TwELL"). Here each CTA compacts its own output tile independently:
 //
 //   GEMM_TWELL_RELU  A = x (tokens), B = W_up (hidden units). One epilogue
 //                    thread owns one token row of the tile; it adds the bias,
