@@ -307,29 +307,28 @@ __global__ void __launch_bounds__(192, 1)
             if constexpr (MODE == GEMM_TWELL_RELU) {
                 epi_twell_row<BN, CAP>(tbase, mb * BM + 32 * q + lane, rowsA, nb, a, bias_sm);
             } else if constexpr (MODE == GEMM_GATE_SWAP) {
+                // Tokens in chunks of 16 accumulator columns under a loop that
+                // is not unrolled: fully unrolled over 64 tokens this code no
+                // longer fit the instruction cache and starved the producer
+                // and MMA threads. TMEM is read twice (masks, then values).
                 const int j = mb * BM + 32 * q + lane;  // hidden unit
                 const bool j_ok = j < a.rowsA;
                 const float bj = j_ok ? a.bias[j] : 0.f;
                 const int ntok = min(BN, a.rowsB);
-                uint32_t v[BN];
-                if constexpr (BN == 16) {
-                    uint32_t (&v16)[16] = *reinterpret_cast<uint32_t(*)[16]>(v);
-                    tmem_ld16_wait(tbase, v16);
-                } else {
-#pragma unroll
-                    for (int ch = 0; ch < BN / 32; ++ch) {
-                        uint32_t (&v32)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + ch * 32);
-                        tmem_ld32_wait(tbase + ch * 32, v32);
-                    }
-                }
                 bool any = false;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16_wait(tbase + c0, v);
 #pragma unroll
-                for (int t = 0; t < BN; ++t) {
-                    if (t < ntok) {
-                        const bool act = j_ok && (__uint_as_float(v[t]) + bj > 0.f);
-                        any |= act;
-                        const uint32_t m = __ballot_sync(0xffffffffu, act);
-                        if (lane == 0) s_mask[t * 4 + q] = m;
+                    for (int u = 0; u < 16; ++u) {
+                        const int t = c0 + u;
+                        if (t < ntok) {
+                            const bool act = j_ok && (__uint_as_float(v[u]) + bj > 0.f);
+                            any |= act;
+                            const uint32_t m = __ballot_sync(0xffffffffu, act);
+                            if (lane == 0) s_mask[t * 4 + q] = m;
+                        }
                     }
                 }
                 if (a.pf_row_bytes > 0) {
@@ -347,24 +346,31 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 named_bar_sync(1, kEpiThreads);
                 const uint32_t lt = lanemask_lt();
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16_wait(tbase + c0, v);
 #pragma unroll
-                for (int t = 0; t < BN; ++t) {
-                    if (t < ntok) {
-                        const uint32_t mq = s_mask[t * 4 + q];
-                        if ((mq >> lane) & 1u) {
-                            int before = __popc(mq & lt);
-                            for (int qq = 0; qq < q; ++qq) before += __popc(s_mask[t * 4 + qq]);
-                            const float g = __uint_as_float(v[t]) + bj;
-                            a.gstage[((size_t)(tok0 + t) * a.NB + mb) * BM + before] =
-                                make_uint2((uint32_t)j, __float_as_uint(g));
-                        }
-                        if (et == 0) {
-                            const int total = __popc(s_mask[t * 4 + 0]) + __popc(s_mask[t * 4 + 1]) +
-                                              __popc(s_mask[t * 4 + 2]) + __popc(s_mask[t * 4 + 3]);
-                            a.stage_cnt[(size_t)(tok0 + t) * a.NB + mb] = total;
-                            if (total && a.nnz) atomicAdd(&a.nnz[tok0 + t], total);
+                    for (int u = 0; u < 16; ++u) {
+                        const int t = c0 + u;
+                        if (t < ntok) {
+                            const uint32_t mq = s_mask[t * 4 + q];
+                            if ((mq >> lane) & 1u) {
+                                int before = __popc(mq & lt);
+                                for (int qq = 0; qq < q; ++qq) before += __popc(s_mask[t * 4 + qq]);
+                                const float g = __uint_as_float(v[u]) + bj;
+                                a.gstage[((size_t)(tok0 + t) * a.NB + mb) * BM + before] =
+                                    make_uint2((uint32_t)j, __float_as_uint(g));
+                            }
                         }
                     }
+                }
+                // per-token counts of this tile, one epilogue thread per token
+                for (int t = et; t < ntok; t += kEpiThreads) {
+                    const int total = __popc(s_mask[t * 4 + 0]) + __popc(s_mask[t * 4 + 1]) +
+                                      __popc(s_mask[t * 4 + 2]) + __popc(s_mask[t * 4 + 3]);
+                    a.stage_cnt[(size_t)(tok0 + t) * a.NB + mb] = total;
+                    if (total && a.nnz) atomicAdd(&a.nnz[tok0 + t], total);
                 }
             } else {  // GEMM_DENSE
                 epi_dense_row<BN>(tbase, mb * BM + 32 * q + lane, rowsA, nb, a, bias_sm);

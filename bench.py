@@ -555,6 +555,71 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
     return out
 
 
+def training_leg(tw, flush, stream, reps: int = 5):
+    """The training workload (16384 tokens, d_model 4096, d_ff 16384, ReLU, bias
+    -2.33, L1 1e-4): one fwd + bwd step through the library, L2 flushed before
+    each, and the dense tcgen05 forward on the same shape. Inputs are drawn on
+    the device (seeded; the distributions of the synthetic generator)."""
+    c = syn.CONFIGS["training"]
+    M, d, F, T = c["M"], c["d"], c["F"], c["T"]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+
+    def bf(shape, scale):
+        return (torch.randn(shape, device="cuda", generator=g) * scale).to(torch.bfloat16).view(torch.int16)
+
+    x, dy = bf((M, d), 1.0), bf((M, d), 1.0)
+    Wu, Wd = bf((F, d), d ** -0.5), bf((F, d), F ** -0.5)
+    b = torch.full((F,), float(c["bias"]), dtype=torch.float32, device="cuda")
+    cap = M * 256  # slot capacity: ~1.3x the expected width at 1 % density
+    buf = tw.TwellBuffers(M, F, T, cap)
+    ws_f = torch.empty(tw.twell_fwd_workspace_bytes(M, d, F, T, cap, STAGE_CAP), dtype=torch.uint8, device="cuda")
+    ws_b = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, cap), dtype=torch.uint8, device="cuda")
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    db = torch.empty(F, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    evs = []
+    for i in range(reps + 2):
+        flush.fill_(i & 0xff)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        tw.twell_ffn_fwd(x, Wu, None, b, Wd, T, buf, y, ws_f, st)
+        e[1].record(stream)
+        tw.twell_ffn_bwd(x, Wu, Wd, buf, dy, float(c["l1"]), dx, dWu, dWd, db, ws_b, st)
+        e[2].record(stream)
+        if i >= 2:
+            evs.append(e)
+    torch.cuda.synchronize()
+    code = tw.twell_check(st)
+    if code != 0:
+        raise RuntimeError(f"training leg: device status {code}: {tw.twell_status_string(code)}")
+    fwd = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    bwd = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+    nnz = int(buf.nnz.sum().item())
+    del ws_b, dWu, dWd
+    WdT = Wd.view(F, d).t().contiguous()
+    hd = torch.empty(M, F, dtype=torch.int16, device="cuda")
+    dts = []
+    for i in range(reps + 2):
+        flush.fill_(i & 0xff)
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        tw.twell_dense_ffn_fwd(x, Wu, b, WdT, hd, y, st)
+        b2.record(stream)
+        if i >= 2:
+            dts.append((a, b2))
+    torch.cuda.synchronize()
+    dense_fwd = statistics.median(a.elapsed_time(b2) for a, b2 in dts)
+    return {"workload": f"M={M}, d_model={d}, d_ff={F}, T={T}, bias={c['bias']}, l1={c['l1']}",
+            "density": nnz / (M * F), "fwd_ms": fwd, "bwd_ms": bwd, "step_ms": fwd + bwd,
+            "tokens_per_s": M / ((fwd + bwd) / 1000.0), "dense_fwd_ms": dense_fwd,
+            "dense_step_estimate_ms": 3 * dense_fwd,
+            "dense_step_note": "3 x the measured dense forward: a dense backward runs each forward GEMM shape twice"}
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import activation_sparse_transformer_tcgen05_gb300 as tw
     from activation_sparse_transformer_tcgen05_gb300 import build as tbuild
@@ -726,6 +791,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         }
     decode = None if args.no_extras else decode_leg(tw, peaks, flush, stream)
     hybrid = None if args.no_extras else hybrid_leg(tw, flush, stream)
+    training = None if args.no_extras else training_leg(tw, flush, stream)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.no_extras:
@@ -753,6 +819,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "kernels": kernels,
         "dense_tcgen05_fwd_ms": dense_ms,
         "hybrid": hybrid,
+        "training": training,
         "energy": energy,
         "memory": memory,
         "decode": decode,
