@@ -188,7 +188,19 @@ def test_fwd_inference_full_size_sampled():
 
 @pytest.mark.parametrize("name", ["decode1", "decode8", "decode64"])
 def test_fwd_gated_decode(name):
-    inp = syn.config_inputs(name)
+    _check_gated(syn.config_inputs(name))
+
+
+@pytest.mark.parametrize("M,d,F,T,seed", [
+    (100, 256, 1024, 32, 4),     # two token chunks of the gate GEMM; layout+fill and slot-parallel up products
+    (300, 264, 1032, 64, 5),     # more than 256 rows: row-parallel up products; ragged d, F and tiles
+    (40, 136, 520, 40, 6),       # a decode batch with ragged d and F (one cooperative tail)
+])
+def test_fwd_gated_beyond_decode(M, d, F, T, seed):
+    _check_gated(syn.ffn_inputs(M, d, F, T, -1.5, seed=seed, gated=True))
+
+
+def _check_gated(inp):
     M, d, F, T = inp.M, inp.d, inp.F, inp.T
     buf, y, st = _fwd(inp)
     _status_ok(st)
