@@ -122,8 +122,13 @@ struct GemmArgs {
     const void* pf1;           //   active units are prefetched into L2 (pf_row_bytes 0: off)
     int pf_row_bytes;
     int NB;                // column blocks of the staging
-    uint16_t* out;         // DENSE output [rowsA, ldo]
+    uint16_t* out;         // DENSE output [rowsA, ldo] bf16
     int ldo;
+    float* out_f32;        // DENSE: if set, fp32 output [rowsA, ldo] instead of out
+    int accumulate;        //   out_f32 += result (else =)
+    const uint16_t* mask;  //   if set, [rowsA, ldm] bf16: result kept only where mask is nonzero
+    int ldm;
+    float add_scalar;      //   added to every result before the mask
     int32_t* status;
 };
 // Returns the column-block width BN the GEMM uses for this mode/shape.

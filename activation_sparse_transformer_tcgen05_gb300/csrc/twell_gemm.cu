@@ -123,7 +123,35 @@ __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int rowsA
     for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t v[32];
         tmem_ld32_wait(tbase + ch * 32, v);
-        if (row_ok) {
+        if (row_ok && a.out_f32) {
+            // fp32 output: + add_scalar, kept where mask is nonzero (if given),
+            // added to what out_f32 holds (if accumulate)
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+                const int col = nb * BN + ch * 32 + g8 * 8;
+                if (col < a.rowsB) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        f[e] = __uint_as_float(v[g8 * 8 + e]) + bias_sm[ch * 32 + g8 * 8 + e] + a.add_scalar;
+                    if (a.mask) {
+                        const uint4 m = *reinterpret_cast<const uint4*>(a.mask + (size_t)row * a.ldm + col);
+                        const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (((mw[e >> 1] >> ((e & 1) * 16)) & 0x7fffu) == 0u) f[e] = 0.f;
+                    }
+                    float4* o = reinterpret_cast<float4*>(a.out_f32 + (size_t)orow * a.ldo + col);
+                    if (a.accumulate) {
+                        const float4 p0 = o[0], p1 = o[1];
+                        f[0] += p0.x; f[1] += p0.y; f[2] += p0.z; f[3] += p0.w;
+                        f[4] += p1.x; f[5] += p1.y; f[6] += p1.z; f[7] += p1.w;
+                    }
+                    o[0] = make_float4(f[0], f[1], f[2], f[3]);
+                    o[1] = make_float4(f[4], f[5], f[6], f[7]);
+                }
+            }
+        } else if (row_ok) {
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const int col = nb * BN + ch * 32 + g8 * 8;

@@ -25,7 +25,7 @@ EXPORTED_SYMBOLS = (
     "twell_pack", "twell_up_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd",
     "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
     "twell_set_kernel_timer", "twell_gather_probe", "twell_hybrid_up_pack", "twell_hybrid_spmm_down",
-    "twell_hybrid_ffn_fwd", "twell_fwd_workspace_bytes",
+    "twell_hybrid_ffn_fwd", "twell_fwd_workspace_bytes", "twell_hybrid_bwd_workspace_bytes", "twell_hybrid_ffn_bwd",
 )
 
 # Call sites of twell_set_kernel_timer.
@@ -102,6 +102,10 @@ def load_library(path: str | None = None):
     lib.twell_hybrid_spmm_down.argtypes = [BUFP, OVP, P, P, I32, P, P, P]
     lib.twell_hybrid_ffn_fwd.restype = I32
     lib.twell_hybrid_ffn_fwd.argtypes = [P, P, P, P, P, I32, I32, I32, I32, BUFP, OVP, P, P, SZ, P, P]
+    lib.twell_hybrid_bwd_workspace_bytes.restype = SZ
+    lib.twell_hybrid_bwd_workspace_bytes.argtypes = [I32, I32, I32, I32, I64, I32]
+    lib.twell_hybrid_ffn_bwd.restype = I32
+    lib.twell_hybrid_ffn_bwd.argtypes = [P, P, P, P, BUFP, OVP, P, I32, F32, P, P, P, P, P, SZ, P, P]
     lib.twell_gather_probe.restype = I32
     lib.twell_gather_probe.argtypes = [P, I32, I32, P, I32, I32, P, P]
     lib.twell_check.restype = I32
@@ -291,6 +295,24 @@ def twell_hybrid_ffn_fwd(x, W_up, b, W_down, W_downT, T: int, h_out: TwellBuffer
         _ptr(W_downT, "W_downT", bytes_per_elem=2, numel=F * d), M, d, F, T, h_out.ref, ov.ref,
         _ptr(y, "y", bytes_per_elem=2, numel=M * d), _ptr(ws, "ws"), ws.numel() * ws.element_size(),
         _ptr(status, "status", bytes_per_elem=4), _stream(stream)), "twell_hybrid_ffn_fwd")
+
+
+def twell_hybrid_bwd_workspace_bytes(M: int, d: int, F: int, T: int, cap_slots: int, cap_rows: int) -> int:
+    return int(load_library().twell_hybrid_bwd_workspace_bytes(M, d, F, T, cap_slots, cap_rows))
+
+
+def twell_hybrid_ffn_bwd(x, W_up, W_down, W_upT, h: TwellBuffers, ov: TwellOverflow, dy, l1: float, dx, dW_up,
+                         dW_down, db, ws, status, stream=None):
+    M, d = x.shape
+    F = h.F
+    _check(load_library().twell_hybrid_ffn_bwd(
+        _ptr(x, "x", bytes_per_elem=2, numel=M * d), _ptr(W_up, "W_up", bytes_per_elem=2, numel=F * d),
+        _ptr(W_down, "W_down", bytes_per_elem=2, numel=F * d), _ptr(W_upT, "W_upT", bytes_per_elem=2, numel=F * d),
+        h.ref, ov.ref, _ptr(dy, "dy", bytes_per_elem=2, numel=M * d), d, float(l1),
+        _ptr(dx, "dx", bytes_per_elem=2, numel=M * d), _ptr(dW_up, "dW_up", bytes_per_elem=4, numel=F * d),
+        _ptr(dW_down, "dW_down", bytes_per_elem=4, numel=F * d), _ptr(db, "db", bytes_per_elem=4, numel=F),
+        _ptr(ws, "ws"), ws.numel() * ws.element_size(), _ptr(status, "status", bytes_per_elem=4), _stream(stream)),
+        "twell_hybrid_ffn_bwd")
 
 
 def twell_ffn_fwd_static_ws(x, W_up, W_gate, b, W_down, T: int, h_out: TwellBuffers, y, status, stream=None):

@@ -505,19 +505,29 @@ HYBRID_C_FRAC = 0.0125
 def hybrid_leg(tw, flush, stream, reps: int = 5):
     """The skewed sweep workloads (8192 tokens, d_model 4096, d_ff 16384, x rows
     scaled by LogNormal(0, 1), gate biases for nominal 90 / 99 / 99.9 %
-    sparsity): forward time and memory of plain TwELL, of the hybrid
-    ELL + dense-overflow format (C = 1.25 % of d_ff) and of the dense layer."""
+    sparsity): forward and backward time and memory of plain TwELL, of the
+    hybrid ELL + dense-overflow format (C = 1.25 % of d_ff) and of the dense
+    layer (forward measured; training step estimated as 3 x the forward)."""
     inp = syn.config_inputs("sweep90")  # the three differ only in the bias
     M, d, F, T = inp.M, inp.d, inp.F, inp.T
     x, Wu, Wd = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_down)
     WdT = Wd.view(F, d).t().contiguous()
+    WuT = Wu.view(F, d).t().contiguous()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    dy = torch.randn(M, d, device="cuda", generator=g).to(torch.bfloat16).view(torch.int16)
     C = round(HYBRID_C_FRAC * F)
+    l1 = 1e-4
     y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    db = torch.empty(F, dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
 
-    def timed(fn):
+    def timed(fn, n=reps):
         evs = []
-        for i in range(reps + 2):
+        for i in range(n + 2):
             flush.fill_(i & 0xff)
             a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -530,7 +540,7 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
             raise RuntimeError(f"hybrid leg: device status {tw.twell_check(st)}")
         return statistics.median(a.elapsed_time(b2) for a, b2 in evs)
 
-    out = {"C": C, "workload": "M=8192, d_model=4096, d_ff=16384, T=128, x rows x LogNormal(0,1)"}
+    out = {"C": C, "workload": "M=8192, d_model=4096, d_ff=16384, T=128, x rows x LogNormal(0,1), l1=1e-4"}
     for name in ("sweep90", "sweep99", "sweep999"):
         b = torch.full((F,), float(syn.CONFIGS[name]["bias"]), dtype=torch.float32, device="cuda")
         buf = tw.TwellBuffers(M, F, T, M * F)
@@ -538,20 +548,32 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
                          device="cuda")
         ms_tw = timed(lambda: tw.twell_ffn_fwd(x, Wu, None, b, Wd, T, buf, y, ws, st))
         slots, nnz = buf.slots(), int(buf.nnz.sum().item())
-        del buf, ws
+        del ws
+        wsb = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, M * F), dtype=torch.uint8,
+                          device="cuda")
+        ms_tw_b = timed(lambda: tw.twell_ffn_bwd(x, Wu, Wd, buf, dy, l1, dx, dWu, dWd, db, wsb, st), n=2)
+        del buf, wsb
         hb = tw.TwellBuffers(M, F, T, M * C)
         ov = tw.TwellOverflow(F, C, M)
         wsh = torch.empty(tw.twell_workspace_bytes(tw.OP_HYBRID_FWD, M, d, F, T, 0), dtype=torch.uint8,
                           device="cuda")
         ms_h = timed(lambda: tw.twell_hybrid_ffn_fwd(x, Wu, b, Wd, WdT, T, hb, ov, y, wsh, st))
         n_ov, ell_slots = int(ov.n_rows.item()), hb.slots()
-        del hb, ov, wsh
+        del wsh
+        wshb = torch.empty(tw.twell_hybrid_bwd_workspace_bytes(M, d, F, T, hb.cap_slots, M), dtype=torch.uint8,
+                           device="cuda")
+        ms_h_b = timed(lambda: tw.twell_hybrid_ffn_bwd(x, Wu, Wd, WuT, hb, ov, dy, l1, dx, dWu, dWd, db, wshb, st))
+        del hb, ov, wshb
         hd = torch.empty(M, F, dtype=torch.int16, device="cuda")
         ms_d = timed(lambda: tw.twell_dense_ffn_fwd(x, Wu, b, WdT, hd, y, st))
         del hd
         out[name] = {"density": nnz / (M * F), "twell_ms": ms_tw, "hybrid_ms": ms_h, "dense_ms": ms_d,
+                     "twell_bwd_ms": ms_tw_b, "hybrid_bwd_ms": ms_h_b,
+                     "twell_step_ms": ms_tw + ms_tw_b, "hybrid_step_ms": ms_h + ms_h_b,
+                     "dense_step_estimate_ms": 3 * ms_d,
                      "twell_MB": slots * 6 / 1e6, "hybrid_MB": (ell_slots * 6 + n_ov * F * 2) / 1e6,
-                     "overflow_rows": n_ov, "hybrid_vs_twell": ms_tw / ms_h, "hybrid_vs_dense": ms_d / ms_h}
+                     "overflow_rows": n_ov, "hybrid_vs_twell": ms_tw / ms_h, "hybrid_vs_dense": ms_d / ms_h,
+                     "hybrid_step_vs_twell_step": (ms_tw + ms_tw_b) / (ms_h + ms_h_b)}
     return out
 
 

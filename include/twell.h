@@ -214,6 +214,26 @@ twell_status twell_hybrid_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const
                                   int32_t* status, void* stream);
 
 /*
+ * twell_hybrid_ffn_bwd — the backward of twell_ffn_bwd (same loss, outputs,
+ * layouts and determinism) for a layer whose forward ran on the hybrid format
+ * (Resumo Técnico §2, "Formato Híbrido para Treinamento"): the TwELL rows of h
+ * through the sparse kernels, the dense overflow rows of ov through tcgen05
+ * GEMMs (dpre of those rows masked by their h, dx rows, and their shares of
+ * dW_up, dW_down and db added to the sparse part's).
+ *   W_upT [d, F] bf16: W_up transposed (K-major operand of the dense dx).
+ *   ws: at least twell_hybrid_bwd_workspace_bytes(M, d, F, T, h->cap_slots,
+ *   ov->cap_rows) bytes, 256-byte aligned. Limits as twell_ffn_bwd.
+ * The overflow rows' dpre enters the GEMMs as the sum of two bf16 parts
+ * (~2^-17 relative), accumulated in fp32.
+ */
+size_t twell_hybrid_bwd_workspace_bytes(int M, int d, int F, int T, int64_t cap_slots, int cap_rows);
+twell_status twell_hybrid_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down,
+                                  const uint16_t* W_upT, const twell_buf* h, const twell_overflow* ov,
+                                  const uint16_t* dy, int d, float l1_coef, uint16_t* dx, float* dW_up,
+                                  float* dW_down, float* db, void* ws, size_t ws_bytes, int32_t* status,
+                                  void* stream);
+
+/*
  * twell_ffn_bwd — backward of L = <dy, y> + l1_coef * sum |h| for the ReLU
  * layer (Resumo Técnico §2, "Técnicas de Treinamento": L1 on the ReLU
  * activations), restricted to the stored entries of h:

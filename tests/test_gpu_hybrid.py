@@ -138,3 +138,64 @@ def test_hybrid_sweep90_full_size_sampled_rows():
     compare_hidden(h_rows, ref["h"], h_rows != 0, ref["active"] != 0, ref["pre"], tau)
     y_rows = host_bf16_bits(y)[pick]
     assert_close_rms(bf16_f64(y_rows), ref["y"], what="y", bf16_out=True)
+
+
+# ------------------------------------------------------------------ backward --
+
+def _hybrid_bwd(inp, h_bits, C, cap_rows, l1):
+    """The hybrid backward on the oracle's own split of h (uploaded), through the C ABI."""
+    from helpers import twell_to_device
+    M, d, F, T = inp.M, inp.d, inp.F, inp.T
+    tw_ref, rows, dense = oracle.hybrid_pack(h_bits, T, C)
+    buf = twell_to_device(tw_ref)
+    ov = tw.TwellOverflow(F, C, cap_rows)
+    n = len(rows)
+    ov.n_rows.fill_(n)
+    if n:
+        ov.rows[:n].copy_(torch.from_numpy(rows.astype(np.int32)))
+        ov.dense[:n * F].copy_(torch.from_numpy(np.ascontiguousarray(dense).view(np.int16).reshape(-1)))
+    dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    db = torch.empty(F, dtype=torch.float32, device="cuda")
+    ws = torch.empty(tw.twell_hybrid_bwd_workspace_bytes(M, d, F, T, buf.cap_slots, cap_rows), dtype=torch.uint8,
+                     device="cuda")
+    st = status_tensor()
+    tw.twell_hybrid_ffn_bwd(dev_bf16(inp.x), dev_bf16(inp.W_up), dev_bf16(inp.W_down),
+                            dev_bf16(np.ascontiguousarray(inp.W_up.T)), buf, ov, dev_bf16(inp.dy), l1, dx, dWu, dWd,
+                            db, ws, st)
+    assert tw.twell_check(st) == 0
+    return n, bf16_f64(host_bf16_bits(dx)), dWu.cpu().numpy(), dWd.cpu().numpy(), db.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,d,F,T,C,cap_extra,l1,seed", [
+    (300, 256, 1024, 32, 60, 0, 1e-3, 2),    # several pair tiles of overflow rows; skewed 10 % density
+    (90, 136, 264, 7, 12, 40, 0.0, 3),       # ragged d and F, room for more rows than overflow
+    (200, 128, 520, 16, 300, 8, 5e-2, 4),    # nothing overflows: the sparse backward alone
+])
+def test_hybrid_backward_matches_oracle(M, d, F, T, C, cap_extra, l1, seed):
+    # the hybrid format is another storage of the same h: the gradients are
+    # the plain backward's, compared with the oracle's on the full h
+    inp = syn.ffn_inputs(M, d, F, T, -1.2816, seed=seed, with_dy=True, row_skew_sigma=1.0)
+    fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, want_y=False)
+    counts = ((fw["h"] & 0x7FFF) != 0).sum(1)
+    cap_rows = int((counts > C).sum()) + cap_extra
+    n, dx, dWu, dWd, db = _hybrid_bwd(inp, fw["h"], C, cap_rows, l1)
+    assert (n > 0) == (C < counts.max())
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, fw["h"], inp.dy))
+    _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1)
+    assert_close_rms(dx, dx_ref, what="dx", bf16_out=True)
+    assert_close_rms(dWu, gu, what="dW_up")
+    assert_close_rms(dWd, gd, what="dW_down")
+    assert_close_rms(db, gb, what="db")
+
+
+def test_hybrid_backward_is_deterministic():
+    inp = syn.ffn_inputs(160, 128, 512, 32, -1.2816, seed=6, with_dy=True, row_skew_sigma=1.0)
+    fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, inp.M, inp.d, inp.F, want_y=False)
+    a = _hybrid_bwd(inp, fw["h"], 40, inp.M, 1e-3)
+    b = _hybrid_bwd(inp, fw["h"], 40, inp.M, 1e-3)
+    assert a[0] > 0
+    for u, v in zip(a[1:], b[1:]):
+        np.testing.assert_array_equal(u, v)
