@@ -172,7 +172,8 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (both
-// K-major), fp32 D, shape M x N (M in {64,128}, N a multiple of 8 or 16).
+// K-major), fp32 D, shape M x N (M = 64 or 128 on one CTA, 256 over a CTA
+// pair with cta_group::2; N a multiple of 16 up to 256).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
 {
     return (1u << 4)                          // D format: f32
