@@ -736,16 +736,18 @@ __global__ void __launch_bounds__(kTailWarps * 32, 1)
                     jl = __ldcg(tw.idx + base + k0 + lane);
                     vb = __ldcg(tw.val + base + k0 + lane);
                 }
+                // 8 W_down rows in flight: a decode task walks its entries
+                // alone, so its time is the number of dependent round trips
                 int u = 0;
-                for (; u + 4 <= m; u += 4) {
-                    uint4 w[4];
+                for (; u + 8 <= m; u += 8) {
+                    uint4 w[8];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 8; ++q) {
                         const int jj = __shfl_sync(0xffffffffu, jl, u + q);
                         w[q] = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) fma8_bf16(acc, __shfl_sync(0xffffffffu, vb, u + q), w[q]);
+                    for (int q = 0; q < 8; ++q) fma8_bf16(acc, __shfl_sync(0xffffffffu, vb, u + q), w[q]);
                 }
                 for (; u < m; ++u) {
                     const int jj = __shfl_sync(0xffffffffu, jl, u);
