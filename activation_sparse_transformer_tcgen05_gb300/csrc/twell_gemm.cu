@@ -38,11 +38,13 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int kEpiThreads = 128;
 
-template <int BN, int STAGES>
+// A stage holds KSUB consecutive 64-deep k-blocks (A then B for each).
+template <int BN, int STAGES, int KSUB = 1>
 struct Layout {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SUB_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = KSUB * SUB_BYTES;
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
     static constexpr int NBARS = 2 * STAGES + 5;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
@@ -53,7 +55,7 @@ struct Layout {
     static constexpr int TOTAL = MASK_OFF + MASK_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                         : (2 * BN <= 256) ? 256 : 512;
-    static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
+    static_assert(SUB_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
 };
 
 __device__ __forceinline__ void fail(int32_t* status, volatile int* abort_flag)
@@ -174,11 +176,11 @@ __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int rowsA
     }
 }
 
-template <int BN, int MODE, int STAGES, int CAP = BN>
+template <int BN, int MODE, int STAGES, int CAP = BN, int KSUB = 1>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a, int tok0)
 {
-    using L = Layout<BN, STAGES>;
+    using L = Layout<BN, STAGES, KSUB>;
     constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -241,15 +243,23 @@ __global__ void __launch_bounds__(192, 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int mb = tile % num_m, nb = tile / num_m;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                // gate GEMM: each tile starts at its own k so that the CTAs do not
+                // all ask for the same few lines of x at once (sum order: per tile)
+                const int rot = MODE == GEMM_GATE_SWAP ? (int)((unsigned)(tile * 5 * KSUB) % (unsigned)num_kb) : 0;
+                for (int kb0 = 0; kb0 < num_kb; kb0 += KSUB) {
+                    const int kb = kb0 + rot < num_kb ? kb0 + rot : kb0 + rot - num_kb;
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     uint8_t* sa = smem + stage * L::STAGE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-                    tma_load_2d(sa, &tmA, kb * BK, mb * BM, &full[stage]);
-                    tma_load_2d(sa + L::A_BYTES, &tmB, kb * BK, nb * BN, &full[stage]);
+#pragma unroll
+                    for (int sub = 0; sub < KSUB; ++sub) {
+                        uint8_t* ss = sa + sub * L::SUB_BYTES;
+                        tma_load_2d(ss, &tmA, (kb + sub) * BK, mb * BM, &full[stage]);
+                        tma_load_2d(ss + L::A_BYTES, &tmB, (kb + sub) * BK, nb * BN, &full[stage]);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -279,18 +289,21 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = 0; kb < num_kb; kb += KSUB) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * L::STAGE_BYTES);
-                    const uint64_t adesc = sw128_kmajor_desc(sa);
-                    const uint64_t bdesc = sw128_kmajor_desc(sa + L::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        umma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb | k) != 0);
+                    for (int sub = 0; sub < KSUB; ++sub) {
+                        const uint32_t sa = smem_u32(smem + stage * L::STAGE_BYTES + sub * L::SUB_BYTES);
+                        const uint64_t adesc = sw128_kmajor_desc(sa);
+                        const uint64_t bdesc = sw128_kmajor_desc(sa + L::A_BYTES);
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            umma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb | sub | k) != 0);
+                    }
                     umma_commit(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -686,13 +699,13 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int K, int box_rows)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE, int STAGES, int CAP = BN>
+template <int BN, int MODE, int STAGES, int CAP = BN, int KSUB = 1>
 cudaError_t run(const uint16_t* A, const uint16_t* B, const GemmArgs& a, int tok0, int sm_count, cudaStream_t s)
 {
-    using L = Layout<BN, STAGES>;
+    using L = Layout<BN, STAGES, KSUB>;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, a.rowsA, a.K, BM) || !make_map(&mb, B, a.rowsB, a.K, BN)) return cudaErrorInvalidValue;
-    auto kern = k_gemm_tc<BN, MODE, STAGES, CAP>;
+    auto kern = k_gemm_tc<BN, MODE, STAGES, CAP, KSUB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e != cudaSuccess) return e;
     const int tiles = ((a.rowsA + BM - 1) / BM) * ((a.rowsB + BN - 1) / BN);
@@ -799,7 +812,12 @@ cudaError_t launch_gemm(int mode, const uint16_t* A, const uint16_t* B, const Ge
                 c.rowsB = a.rowsB - t0 < 64 ? a.rowsB - t0 : 64;
                 const uint16_t* Bc = B + (size_t)t0 * a.K;
                 cudaError_t e;
-                if (bn == 16)
+                const int num_kb = (a.K + BK - 1) / BK;
+                if (bn == 16 && num_kb % 4 == 0)
+                    // four consecutive k-blocks per stage: 512 contiguous bytes of
+                    // each W_gate row per stage
+                    e = run<16, GEMM_GATE_SWAP, 3, 16, 4>(A, Bc, c, t0, sm_count, s);
+                else if (bn == 16)
                     e = run<16, GEMM_GATE_SWAP, 11>(A, Bc, c, t0, sm_count, s);
                 else if (bn == 32)
                     e = run<32, GEMM_GATE_SWAP, 8>(A, Bc, c, t0, sm_count, s);
