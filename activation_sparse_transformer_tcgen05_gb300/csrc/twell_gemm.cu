@@ -819,8 +819,12 @@ cudaError_t launch_gemm(int mode, const uint16_t* A, const uint16_t* B, const Ge
                     e = run<16, GEMM_GATE_SWAP, 3, 16, 4>(A, Bc, c, t0, sm_count, s);
                 else if (bn == 16)
                     e = run<16, GEMM_GATE_SWAP, 11>(A, Bc, c, t0, sm_count, s);
+                else if (bn == 32 && num_kb % 2 == 0)
+                    e = run<32, GEMM_GATE_SWAP, 5, 32, 2>(A, Bc, c, t0, sm_count, s);
                 else if (bn == 32)
                     e = run<32, GEMM_GATE_SWAP, 8>(A, Bc, c, t0, sm_count, s);
+                else if (num_kb % 2 == 0)
+                    e = run<64, GEMM_GATE_SWAP, 4, 64, 2>(A, Bc, c, t0, sm_count, s);
                 else
                     e = run<64, GEMM_GATE_SWAP, 8>(A, Bc, c, t0, sm_count, s);
                 if (e != cudaSuccess) return e;
