@@ -310,11 +310,11 @@ def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:
 # the SHA-256 of the source file it was built from: once that file changes the
 # figure no longer describes the kernel and the site reports traffic null.
 NCU_TRAFFIC = {
-    1: ("twell_gemm.cu", "f713d35da43c5c8dd2ae901c127d1caa008c7a0d49ade5e9957f124ff5b9aeee", 53.066752e6),
-    2: ("twell_sparse.cu", "c95dca8eaaa28a4a14783e03be041b75164c36fb79c9ec871ecb1a941b4e86ee", 37.872896e6),
-    3: ("twell_sparse.cu", "c95dca8eaaa28a4a14783e03be041b75164c36fb79c9ec871ecb1a941b4e86ee", 52.562432e6),
-    4: ("twell_sparse.cu", "c95dca8eaaa28a4a14783e03be041b75164c36fb79c9ec871ecb1a941b4e86ee", 39.017216e6),
-    6: ("twell_sparse.cu", "c95dca8eaaa28a4a14783e03be041b75164c36fb79c9ec871ecb1a941b4e86ee", 136.225024e6),
+    1: ("twell_gemm.cu", "26dfe7157735f1512e423b5748429ec2141ba9124d9bd14beb4892b356f8ab92", 52.983808e6),
+    2: ("twell_sparse.cu", "37ce152fcac6eb984779176ed321ed0ad76738ea6d0d69a02f0d359df6a59af4", 37.75488e6),
+    3: ("twell_sparse.cu", "37ce152fcac6eb984779176ed321ed0ad76738ea6d0d69a02f0d359df6a59af4", 52.667648e6),
+    4: ("twell_sparse.cu", "37ce152fcac6eb984779176ed321ed0ad76738ea6d0d69a02f0d359df6a59af4", 39.082752e6),
+    6: ("twell_sparse.cu", "37ce152fcac6eb984779176ed321ed0ad76738ea6d0d69a02f0d359df6a59af4", 135.439104e6),
 }
 
 
