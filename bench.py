@@ -145,6 +145,22 @@ def oracle_rate(inp: syn.FFNInputs, budget_s: float):
     return done / dt, S, dt, oracle.num_threads(), done
 
 
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest of the ranks' values: the job's step time is its slowest
+    replica's. Collective over the initialised process group when world > 1."""
+    if world <= 1:
+        return value
+    on_gpu = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_replica: int, world: int, ms_step: float) -> float:
+    """Tokens per second of the whole job: every replica processes its own batch."""
+    return world * tokens_per_replica / (ms_step / 1000.0)
+
+
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
@@ -721,12 +737,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     down = [e[1].elapsed_time(e[2]) for e in events]
     bwd = [e[2].elapsed_time(e[3]) for e in events]
     ms = {"up_pack": statistics.mean(up), "spmm_down": statistics.mean(down), "ffn_bwd": statistics.mean(bwd)}
-    ms_step = sum(ms.values())
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * inp.M / (ms_step / 1000.0)
+    ms_step = max_over_ranks(sum(ms.values()), world)
+    value = whole_job_rate(inp.M, world, ms_step)
     ms_fwd = ms["up_pack"] + ms["spmm_down"]
 
     stages = {k: dict(ms=v, **stage_roofline(k, v, inp, slots, nnz, peaks)) for k, v in ms.items()}
