@@ -102,6 +102,8 @@ enum GemmMode { GEMM_TWELL_RELU = 0, GEMM_GATE_SWAP = 1, GEMM_DENSE = 2 };
 // down-projection in one cooperative launch; y == nullptr skips the
 // down-projection. `counter` must be 0 when it starts (grid barrier).
 bool decode_tail_ok(int M, int NB, int n_tiles);
+// Bounded-wait self-test: which 0 = mbarrier, 1 = grid barrier (*counter must be 0).
+cudaError_t launch_wait_selftest(int which, int32_t* counter, int32_t* status, cudaStream_t s);
 cudaError_t launch_decode_tail(const uint2* gstage, const int32_t* stage_cnt, int NB, int BM, const uint16_t* x,
                                const uint16_t* W_up, const uint16_t* W_down, int d, const TwellView& tw,
                                uint16_t* y, int32_t* counter, int32_t* status, cudaStream_t s);

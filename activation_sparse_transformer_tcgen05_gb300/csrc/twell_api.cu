@@ -523,6 +523,15 @@ twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end)
 
 int64_t twell_kernel_launches(void) { return (int64_t)g_kernel_launches.load(std::memory_order_relaxed); }
 
+twell_status twell_wait_selftest(int which, int32_t* scratch, int32_t* status, void* stream)
+{
+    if ((which != 0 && which != 1) || !scratch || !status) return TWELL_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = launch_wait_selftest(which, scratch, status, s);
+    return cuda_status(e);
+}
+
 twell_status twell_check(const int32_t* status, void* stream, int32_t* host_status)
 {
     if (!status || !host_status) return TWELL_ERR_INVALID_ARG;

@@ -573,6 +573,51 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p)
     return v;
 }
 
+// Grid-wide barrier of a cooperative launch: every block adds one to *counter
+// and waits until it reaches `target`. Bounded: after kWaitLimitNs without
+// getting there it returns false (in every thread of the block) instead of
+// waiting on. `flag` is a shared int of the block.
+__device__ __forceinline__ bool grid_barrier(int32_t* counter, int target, int* flag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(counter, 1);
+        const uint64_t t0 = globaltimer_ns();
+        int go = 1;
+        while (ld_acquire_gpu(counter) < target) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                go = 0;
+                break;
+            }
+        }
+        *flag = go;
+    }
+    __syncthreads();
+    return *flag != 0;
+}
+
+// Self-test of the bounded waits (twell_wait_selftest): a wait that nothing
+// will complete runs out and reports TWELL_ERR_TIMEOUT. which = 0: an
+// mbarrier nobody arrives on; which = 1: the grid barrier with a target the
+// grid cannot reach.
+__global__ void k_wait_selftest(int which, int32_t* counter, int32_t* status)
+{
+    __shared__ uint64_t bar;
+    __shared__ int flag;
+    if (which == 0) {
+        if (threadIdx.x == 0) {
+            mbar_init(&bar, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0 && !mbar_wait(&bar, 0, nullptr)) set_error(status, TWELL_ERR_TIMEOUT);
+    } else {
+        if (!grid_barrier(counter, (int)gridDim.x + 1, &flag) && threadIdx.x == 0)
+            set_error(status, TWELL_ERR_TIMEOUT);
+    }
+}
+
 __global__ void __launch_bounds__(kTailWarps * 32, 1)
     k_decode_tail(const uint2* __restrict__ gstage, const int32_t* __restrict__ stage_cnt, int NB, int BM,
                   const uint16_t* __restrict__ x, const uint16_t* __restrict__ W_up,
@@ -687,22 +732,7 @@ __global__ void __launch_bounds__(kTailWarps * 32, 1)
     if (!y) return;
 
     // ------------------------------------------------------ grid barrier --
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        atomicAdd(counter, 1);
-        const uint64_t t0 = globaltimer_ns();
-        int go = 1;
-        while (ld_acquire_gpu(counter) < (int)gridDim.x) {
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                go = 0;
-                break;
-            }
-        }
-        s_go = go;
-    }
-    __syncthreads();
-    if (!s_go) {
+    if (!grid_barrier(counter, (int)gridDim.x, &s_go)) {
         if (tid == 0) set_error(status, TWELL_ERR_TIMEOUT);
         return;
     }
@@ -1331,6 +1361,15 @@ cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16
 }
 
 bool small_fill_ok(int M, int NB) { return M <= 1024 && (long long)M * NB <= kSmallFillMax; }
+
+cudaError_t launch_wait_selftest(int which, int32_t* counter, int32_t* status, cudaStream_t s)
+{
+    count_launches(1);
+    // one block for the mbarrier case; a small grid for the barrier (all blocks
+    // resident at once, as the cooperative launch of the decode tail guarantees)
+    k_wait_selftest<<<which == 0 ? 1 : 4, 64, 0, s>>>(which, counter, status);
+    return cudaGetLastError();
+}
 
 int decode_tail_grid()
 {

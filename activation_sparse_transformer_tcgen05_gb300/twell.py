@@ -26,6 +26,7 @@ EXPORTED_SYMBOLS = (
     "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
     "twell_set_kernel_timer", "twell_gather_probe", "twell_hybrid_up_pack", "twell_hybrid_spmm_down",
     "twell_hybrid_ffn_fwd", "twell_fwd_workspace_bytes", "twell_hybrid_bwd_workspace_bytes", "twell_hybrid_ffn_bwd",
+    "twell_wait_selftest",
 )
 
 # Call sites of twell_set_kernel_timer.
@@ -108,6 +109,8 @@ def load_library(path: str | None = None):
     lib.twell_hybrid_ffn_bwd.argtypes = [P, P, P, P, BUFP, OVP, P, I32, F32, P, P, P, P, P, SZ, P, P]
     lib.twell_gather_probe.restype = I32
     lib.twell_gather_probe.argtypes = [P, I32, I32, P, I32, I32, P, P]
+    lib.twell_wait_selftest.restype = I32
+    lib.twell_wait_selftest.argtypes = [I32, P, P, P]
     lib.twell_check.restype = I32
     lib.twell_check.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     _lib = lib
@@ -235,6 +238,13 @@ def twell_gather_probe(W: torch.Tensor, idx: torch.Tensor, sink: torch.Tensor, s
         _ptr(W, "W", bytes_per_elem=2, numel=F * d), F, d, _ptr(idx, "idx", bytes_per_elem=4, numel=rows * nnz),
         rows, nnz, _ptr(sink, "sink", bytes_per_elem=4, numel=rows * ((d + 255) // 256)), _stream(stream)),
         "twell_gather_probe")
+
+
+def twell_wait_selftest(which: int, scratch, status, stream=None):
+    """A bounded wait that runs out (about 1 s) and reports TWELL_ERR_TIMEOUT in status."""
+    _check(load_library().twell_wait_selftest(int(which), _ptr(scratch, "scratch", bytes_per_elem=4, numel=1),
+                                              _ptr(status, "status", bytes_per_elem=4), _stream(stream)),
+           "twell_wait_selftest")
 
 
 def twell_up_pack(x, W_up, W_gate, b, T: int, h_out: TwellBuffers, ws, status, stream=None):

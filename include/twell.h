@@ -316,6 +316,19 @@ enum { TWELL_SITE_NONE = 0, TWELL_SITE_UP_GEMM = 1, TWELL_SITE_SPMM_DOWN = 2, TW
 twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end);
 
 /*
+ * twell_wait_selftest — diagnostic of the library's bounded waits: runs a
+ * wait that nothing will complete, with the same helpers the kernels use
+ * (which = 0: an mbarrier no thread arrives on; which = 1: the decode tail's
+ * grid barrier with a target the grid cannot reach). After its limit (about
+ * one second) the wait gives up and writes TWELL_ERR_TIMEOUT to *status
+ * (first error sticks); the CUDA context stays usable.
+ *   scratch: one int32 of device memory (zeroed by the call).
+ * Asynchronous on `stream`; TWELL_ERR_INVALID_ARG for another `which` or null
+ * pointers.
+ */
+twell_status twell_wait_selftest(int which, int32_t* scratch, int32_t* status, void* stream);
+
+/*
  * twell_gather_probe — measurement aid: the memory access pattern of the
  * library's sparse kernels without their arithmetic, so that their time can be
  * set against the gather rate of the GPU they run on. One warp per (row r,

@@ -71,6 +71,8 @@ def test_host_argument_errors_need_no_gpu(lib):
     rc = lib.twell_gather_probe(fake, 8192, 2044, fake, 4096, 82, fake, None)
     assert rc == 1
     assert lib.twell_set_kernel_timer(9, None, None) == 1  # no such call site
+    assert lib.twell_wait_selftest(2, fake, fake, None) == 1  # no such wait
+    assert lib.twell_wait_selftest(0, None, None, None) == 1
 
 
 def test_ops_fail_loudly_without_library(tmp_path):
