@@ -842,6 +842,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "config": {"workload": WORKLOAD, "M": inp.M, "d_model": inp.d, "d_ff": inp.F, "T": inp.T, "bias": -2.33,
                    "l1": L1, "l2": "flushed between timed steps (512 MB write, then 512 MB read: clean lines)",
                    "parallelism": f"replicas x{world}", "measured_density": nnz / (inp.M * inp.F),
+                   "padding_ratio": slots / max(nnz, 1),
                    "slots": slots},
         "roofline": roof,
         "cpu_baseline": cpu,
