@@ -86,11 +86,13 @@ struct CscWork {
     int32_t* start;             // [row_blocks, F]
     int32_t* colcnt;            // [F]
     int32_t* colptr;            // [F + 1]
-    int32_t* crow;              // [cap]
-    int32_t* cslot;             // [cap]
+    int32_t* crow;              // [cap] row of each column-list entry
+    uint16_t* cval;             // [cap] its h (bf16)
+    float* cdpre;               // [cap] its dpre
 };
 void csc_plan(int M, int F, int* row_blocks, int* rows_per_block);
-cudaError_t launch_csc(const TwellView& tw, const CscWork& w, int32_t* status, cudaStream_t s);
+// Column lists of the stored entries with their row, h and dpre (dpre: [slots], by slot).
+cudaError_t launch_csc(const TwellView& tw, const CscWork& w, const float* dpre, int32_t* status, cudaStream_t s);
 // dW_down[j] = sum h dy[r], dW_up[j] = sum dpre x[r], db[j] = sum dpre over column j.
 cudaError_t launch_wgrad(const TwellView& tw, const CscWork& w, const float* dpre, const uint16_t* x,
                          const uint16_t* dy, int d, float* dW_up, float* dW_down, float* db, int32_t* status,

@@ -93,7 +93,8 @@ size_t carve_bwd(void* ws, int M, int F, int64_t cap, BwdWs* out)
     w.csc.colcnt = c.take<int32_t>((size_t)F);
     w.csc.colptr = c.take<int32_t>((size_t)F + 1);
     w.csc.crow = c.take<int32_t>(capn);
-    w.csc.cslot = c.take<int32_t>(capn);
+    w.csc.cval = c.take<uint16_t>(capn);
+    w.csc.cdpre = c.take<float>(capn);
     if (out) *out = w;
     return c.used;
 }
@@ -472,7 +473,7 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
     if (e == cudaSuccess) e = launch_spmm_rows(tw, w.dpre, W_up, d, dx, status, s);
     timer_end(TWELL_SITE_DX, s);
     timer_begin(TWELL_SITE_CSC, s);
-    if (e == cudaSuccess) e = launch_csc(tw, w.csc, status, s);
+    if (e == cudaSuccess) e = launch_csc(tw, w.csc, w.dpre, status, s);
     timer_end(TWELL_SITE_CSC, s);
     timer_begin(TWELL_SITE_WGRAD, s);
     if (e == cudaSuccess) e = launch_wgrad(tw, w.csc, w.dpre, x, dy, d, dW_up, dW_down, db, status, s);

@@ -1131,9 +1131,13 @@ __global__ void __launch_bounds__(1024) k_scan_i32(const int32_t* __restrict__ c
     if (tid == 1023) ptr[n] = run;
 }
 
+// Each entry goes to its place in its column's list with its row, its h and
+// its dpre: the weight-gradient kernel then reads them with coalesced loads
+// instead of every one of its column-group warps gathering them by slot.
 __global__ void k_csc_scatter(TwellView tw, const unsigned long long* __restrict__ masks,
                               const int32_t* __restrict__ start, const int32_t* __restrict__ colptr,
-                              int32_t* __restrict__ crow, int32_t* __restrict__ cslot, const int32_t* status)
+                              const float* __restrict__ dpre, int32_t* __restrict__ crow,
+                              uint16_t* __restrict__ cval, float* __restrict__ cdpre, const int32_t* status)
 {
     const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -1148,7 +1152,8 @@ __global__ void k_csc_scatter(TwellView tw, const unsigned long long* __restrict
         const size_t bj = (size_t)b * tw.F + j;
         const int pos = colptr[j] + start[bj] + __popcll(masks[bj] & below);
         crow[pos] = r;
-        cslot[pos] = (int32_t)(base + k);
+        cval[pos] = tw.val[base + k];
+        cdpre[pos] = dpre[base + k];
     }
 }
 
@@ -1157,8 +1162,8 @@ __global__ void k_csc_scatter(TwellView tw, const unsigned long long* __restrict
 // column's entries in row order; db[j] by the group-0 warp.
 __global__ void __launch_bounds__(kWarps * 32) k_wgrad(TwellView tw, const int32_t* __restrict__ colptr,
                                                        const int32_t* __restrict__ crow,
-                                                       const int32_t* __restrict__ cslot,
-                                                       const float* __restrict__ dpre,
+                                                       const uint16_t* __restrict__ cval,
+                                                       const float* __restrict__ cdpre,
                                                        const uint16_t* __restrict__ x,
                                                        const uint16_t* __restrict__ dy, int d,
                                                        float* __restrict__ dW_up, float* __restrict__ dW_down,
@@ -1183,9 +1188,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_wgrad(TwellView tw, const int32
         float pl = 0.f;
         if (lane < m) {
             rl = crow[b0 + lane];
-            const int s = cslot[b0 + lane];
-            hl = tw.val[s];
-            pl = dpre[s];
+            hl = cval[b0 + lane];
+            pl = cdpre[b0 + lane];
         }
         bsum += pl;
         int u = 0;
@@ -1445,7 +1449,7 @@ void csc_plan(int M, int F, int* row_blocks, int* rows_per_block)
     *row_blocks = (M + kCscRows - 1) / kCscRows;
 }
 
-cudaError_t launch_csc(const TwellView& tw, const CscWork& w, int32_t* status, cudaStream_t s)
+cudaError_t launch_csc(const TwellView& tw, const CscWork& w, const float* dpre, int32_t* status, cudaStream_t s)
 {
     // split the columns so that the mask pass has at least two blocks per SM
     int splits = (2 * 152 + w.row_blocks - 1) / w.row_blocks;
@@ -1462,8 +1466,8 @@ cudaError_t launch_csc(const TwellView& tw, const CscWork& w, int32_t* status, c
     k_csc_mask<<<dim3(w.row_blocks, ny), 256, smem, s>>>(tw, col_range, w.masks, status);
     k_csc_colscan<<<(tw.F + 31) / 32, 1024, 0, s>>>(w.masks, w.row_blocks, tw.F, w.start, w.colcnt, status);
     k_scan_i32<<<1, 1024, 0, s>>>(w.colcnt, tw.F, w.colptr, status);
-    k_csc_scatter<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, w.masks, w.start, w.colptr, w.crow, w.cslot,
-                                                               status);
+    k_csc_scatter<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, w.masks, w.start, w.colptr, dpre, w.crow,
+                                                               w.cval, w.cdpre, status);
     return cudaGetLastError();
 }
 
@@ -1473,7 +1477,8 @@ cudaError_t launch_wgrad(const TwellView& tw, const CscWork& w, const float* dpr
 {
     const int64_t tasks = (int64_t)tw.F * ((d + 255) / 256);
     count_launches(1);
-    k_wgrad<<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, w.colptr, w.crow, w.cslot, dpre, x, dy, d, dW_up,
+    (void)dpre;  // carried in the column lists
+    k_wgrad<<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, w.colptr, w.crow, w.cval, w.cdpre, x, dy, d, dW_up,
                                                           dW_down, db, status);
     return cudaGetLastError();
 }
