@@ -135,6 +135,21 @@ struct GemmArgs {
     float add_scalar;      //   added to every result before the mask
     int32_t* status;
 };
+// ---- Down-projection on the tensor cores over token-group unions (twell_union.cu)
+struct UnionWork {
+    int32_t* ucnt;     // [groups] |U| of each 128-token group
+    int32_t* ulist;    // [groups * F + 64] ascending active units of each group
+    int32_t* kbptr;    // [groups, kb_stride] bucket starts per 64-deep k-block of U
+    int kb_stride;     // union_kb_stride(F)
+    int64_t* gbase;    // [groups] first TwELL slot of the group
+    uint32_t* ent;     // [cap + 4] bucketed entries (bf16 | pos % 64 << 16 | row << 22)
+};
+int union_kb_stride(int F);
+size_t union_smem_bytes(int F);  // shared memory of the GEMM kernel
+cudaError_t launch_union_build(const TwellView& tw, const UnionWork& w, int32_t* status, cudaStream_t s);
+cudaError_t launch_spmm_union(const TwellView& tw, const uint16_t* W, int d, const UnionWork& w, uint16_t* y,
+                              int32_t* status, cudaStream_t s);
+
 // Returns the column-block width BN the GEMM uses for this mode/shape.
 int gemm_block_n(int mode, int rowsB);
 cudaError_t launch_gemm(int mode, const uint16_t* A, const uint16_t* B, const GemmArgs& a, int sm_count,

@@ -99,6 +99,22 @@ size_t carve_bwd(void* ws, int M, int F, int64_t cap, BwdWs* out)
     return c.used;
 }
 
+// Workspace of the union down-projection; 16-byte aligned pieces.
+size_t carve_union(void* ws, int M, int F, int64_t cap, UnionWork* out)
+{
+    Carver c{static_cast<char*>(ws)};
+    UnionWork w{};
+    const size_t ng = (size_t)((M + 127) / 128);
+    w.kb_stride = union_kb_stride(F);
+    w.ucnt = c.take<int32_t>(ng);
+    w.gbase = c.take<int64_t>(ng);
+    w.kbptr = c.take<int32_t>(ng * (size_t)w.kb_stride);
+    w.ulist = c.take<int32_t>(ng * (size_t)F + 64);
+    w.ent = c.take<uint32_t>((size_t)(cap > 0 ? cap : 0) + 4);
+    if (out) *out = w;
+    return c.used;
+}
+
 twell_status check_buf(const twell_buf* b, int M, int F, int T)
 {
     if (!b) return TWELL_ERR_INVALID_ARG;
@@ -131,6 +147,7 @@ bool dims_ok(int M, int d, int F) { return M > 0 && d > 0 && F > 0 && d % 8 == 0
 
 // Limits of this build's kernels.
 constexpr int kMaxD = 4096;  // the gated up products keep 16 chunks of 256 columns per warp in registers
+constexpr int kUnionMaxF = 65536;  // the union kernel keeps a group's bucket starts in shared memory
 
 }  // namespace
 
@@ -222,6 +239,37 @@ twell_status twell_spmm_down(const twell_buf* h, const uint16_t* W_down, int d, 
     timer_begin(TWELL_SITE_SPMM_DOWN, s);
     const cudaError_t e = launch_spmm_rows(tw, nullptr, W_down, d, y, status, s);
     timer_end(TWELL_SITE_SPMM_DOWN, s);
+    return cuda_status(e);
+}
+
+size_t twell_spmm_down_tc_workspace_bytes(int M, int F, int64_t cap_slots)
+{
+    if (M <= 0 || F <= 0 || F % 8 != 0 || F > kUnionMaxF || cap_slots < 0) return 0;
+    return carve_union(nullptr, M, F, cap_slots, nullptr);
+}
+
+twell_status twell_spmm_down_tc(const twell_buf* h, const uint16_t* W_down, int d, uint16_t* y, void* ws,
+                                size_t ws_bytes, int32_t* status, void* stream)
+{
+    if (!h || !W_down || !y || !status || d <= 0 || d % 8 != 0 || !aligned16(W_down) || !aligned16(y))
+        return TWELL_ERR_INVALID_ARG;
+    if (h->M <= 0 || h->F <= 0 || h->F % 8 != 0) return TWELL_ERR_INVALID_ARG;
+    twell_status st = check_buf(h, h->M, h->F, h->T);
+    if (st != TWELL_OK) return st;
+    if (h->F > kUnionMaxF) return TWELL_ERR_UNSUPPORTED;
+    if (!ws) return TWELL_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;
+    if (ws_bytes < carve_union(nullptr, h->M, h->F, h->cap_slots, nullptr)) return TWELL_ERR_WORKSPACE;
+    UnionWork w;
+    carve_union(ws, h->M, h->F, h->cap_slots, &w);
+    const TwellView tw = view_of(h);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    timer_begin(TWELL_SITE_SPMM_UNION, s);
+    timer_begin(TWELL_SITE_UNION_BUILD, s);
+    cudaError_t e = launch_union_build(tw, w, status, s);
+    timer_end(TWELL_SITE_UNION_BUILD, s);
+    if (e == cudaSuccess) e = launch_spmm_union(tw, W_down, d, w, y, status, s);
+    timer_end(TWELL_SITE_SPMM_UNION, s);
     return cuda_status(e);
 }
 
@@ -515,7 +563,7 @@ twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const 
 
 twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end)
 {
-    if (site < TWELL_SITE_NONE || site > TWELL_SITE_OVERFLOW_GEMM) return TWELL_ERR_INVALID_ARG;
+    if (site < TWELL_SITE_NONE || site > TWELL_SITE_UNION_BUILD) return TWELL_ERR_INVALID_ARG;
     g_timer.site = (ev_begin && ev_end) ? site : TWELL_SITE_NONE;
     g_timer.begin = static_cast<cudaEvent_t>(ev_begin);
     g_timer.end = static_cast<cudaEvent_t>(ev_end);

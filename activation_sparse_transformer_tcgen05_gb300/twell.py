@@ -26,12 +26,12 @@ EXPORTED_SYMBOLS = (
     "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
     "twell_set_kernel_timer", "twell_gather_probe", "twell_hybrid_up_pack", "twell_hybrid_spmm_down",
     "twell_hybrid_ffn_fwd", "twell_fwd_workspace_bytes", "twell_hybrid_bwd_workspace_bytes", "twell_hybrid_ffn_bwd",
-    "twell_wait_selftest",
+    "twell_wait_selftest", "twell_spmm_down_tc_workspace_bytes", "twell_spmm_down_tc",
 )
 
 # Call sites of twell_set_kernel_timer.
 (SITE_NONE, SITE_UP_GEMM, SITE_SPMM_DOWN, SITE_SDDMM, SITE_DX, SITE_CSC, SITE_WGRAD, SITE_DECODE_TAIL,
- SITE_OVERFLOW_GEMM) = range(9)
+ SITE_OVERFLOW_GEMM, SITE_SPMM_UNION, SITE_UNION_BUILD) = range(11)
 
 # Size of the library-owned workspace behind twell_ffn_fwd_static_ws.
 STATIC_WS_BYTES = 32 * 1024 * 1024
@@ -89,6 +89,10 @@ def load_library(path: str | None = None):
     lib.twell_set_kernel_timer.argtypes = [I32, P, P]
     lib.twell_spmm_down.restype = I32
     lib.twell_spmm_down.argtypes = [BUFP, P, I32, P, P, P]
+    lib.twell_spmm_down_tc_workspace_bytes.restype = SZ
+    lib.twell_spmm_down_tc_workspace_bytes.argtypes = [I32, I32, I64]
+    lib.twell_spmm_down_tc.restype = I32
+    lib.twell_spmm_down_tc.argtypes = [BUFP, P, I32, P, P, SZ, P, P]
     lib.twell_ffn_fwd.restype = I32
     lib.twell_ffn_fwd.argtypes = [P, P, P, P, P, I32, I32, I32, I32, BUFP, P, P, SZ, P, P]
     lib.twell_ffn_bwd.restype = I32
@@ -263,6 +267,21 @@ def twell_spmm_down(h: TwellBuffers, W_down: torch.Tensor, y: torch.Tensor, stat
                                           _ptr(y, "y", bytes_per_elem=2, numel=h.M * d),
                                           _ptr(status, "status", bytes_per_elem=4), _stream(stream)),
            "twell_spmm_down")
+
+
+def twell_spmm_down_tc_workspace_bytes(M: int, F: int, cap_slots: int) -> int:
+    return int(load_library().twell_spmm_down_tc_workspace_bytes(M, F, cap_slots))
+
+
+def twell_spmm_down_tc(h: TwellBuffers, W_down: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
+                       status: torch.Tensor, stream=None):
+    """y = h W_down on the tensor cores over each 128-token group's union of active units."""
+    d = W_down.shape[1]
+    _check(load_library().twell_spmm_down_tc(h.ref, _ptr(W_down, "W_down", bytes_per_elem=2, numel=h.F * d), d,
+                                             _ptr(y, "y", bytes_per_elem=2, numel=h.M * d), _ptr(ws, "ws"),
+                                             ws.numel() * ws.element_size(),
+                                             _ptr(status, "status", bytes_per_elem=4), _stream(stream)),
+           "twell_spmm_down_tc")
 
 
 def twell_ffn_fwd(x, W_up, W_gate, b, W_down, T: int, h_out: TwellBuffers, y, ws, status, stream=None):

@@ -326,11 +326,11 @@ def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:
 # the SHA-256 of the source file it was built from: once that file changes the
 # figure no longer describes the kernel and the site reports traffic null.
 NCU_TRAFFIC = {
-    1: ("twell_gemm.cu", "26dfe7157735f1512e423b5748429ec2141ba9124d9bd14beb4892b356f8ab92", 52.983808e6),
-    2: ("twell_sparse.cu", "37ce152fcac6eb984779176ed321ed0ad76738ea6d0d69a02f0d359df6a59af4", 37.75488e6),
-    3: ("twell_sparse.cu", "37ce152fcac6eb984779176ed321ed0ad76738ea6d0d69a02f0d359df6a59af4", 52.667648e6),
-    4: ("twell_sparse.cu", "37ce152fcac6eb984779176ed321ed0ad76738ea6d0d69a02f0d359df6a59af4", 39.082752e6),
-    6: ("twell_sparse.cu", "37ce152fcac6eb984779176ed321ed0ad76738ea6d0d69a02f0d359df6a59af4", 135.439104e6),
+    1: ("twell_gemm.cu", "26dfe7157735f1512e423b5748429ec2141ba9124d9bd14beb4892b356f8ab92", 53.190912e6),
+    2: ("twell_sparse.cu", "f46042fdf24ecd8ce915e7c89d019d39a9e6af6e77a3f317713719cfa19ecb30", 37.771264e6),
+    3: ("twell_sparse.cu", "f46042fdf24ecd8ce915e7c89d019d39a9e6af6e77a3f317713719cfa19ecb30", 52.516608e6),
+    4: ("twell_sparse.cu", "f46042fdf24ecd8ce915e7c89d019d39a9e6af6e77a3f317713719cfa19ecb30", 38.86336e6),
+    6: ("twell_sparse.cu", "f46042fdf24ecd8ce915e7c89d019d39a9e6af6e77a3f317713719cfa19ecb30", 132.71808e6),
 }
 
 
@@ -518,6 +518,46 @@ def decode_leg(tw, peaks, flush, stream, reps: int = 30):
 HYBRID_C_FRAC = 0.0125
 
 
+def down_variants(tw, buf, Wd, y, st, flush, stream, reps: int = 5):
+    """The down-projection of one TwELL two ways, L2 flushed before each call:
+    the row gather on the CUDA cores (twell_spmm_down) and the tensor-core
+    product over 128-token group unions (twell_spmm_down_tc, both its kernels)."""
+    ws = torch.empty(tw.twell_spmm_down_tc_workspace_bytes(buf.M, buf.F, buf.cap_slots), dtype=torch.uint8,
+                     device="cuda")
+
+    def timed(fn):
+        evs = []
+        for i in range(reps + 2):
+            flush.fill_(i & 0xff)
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b2.record(stream)
+            if i >= 2:
+                evs.append((a, b2))
+        torch.cuda.synchronize()
+        code = tw.twell_check(st)
+        if code != 0:
+            raise RuntimeError(f"down variants: device status {code}: {tw.twell_status_string(code)}")
+        return statistics.median(a.elapsed_time(b2) for a, b2 in evs) * 1000.0
+
+    rows_us = timed(lambda: tw.twell_spmm_down(buf, Wd, y, st))
+    tc_us = timed(lambda: tw.twell_spmm_down_tc(buf, Wd, y, ws, st))
+    a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    b2.record(stream)
+    build = []
+    for i in range(3):
+        flush.fill_(i & 0xff)
+        tw.twell_set_kernel_timer(tw.twell.SITE_UNION_BUILD, a, b2)
+        tw.twell_spmm_down_tc(buf, Wd, y, ws, st)
+        tw.twell_set_kernel_timer(0)
+        torch.cuda.synchronize()
+        build.append(a.elapsed_time(b2) * 1000.0)
+    return {"rows_us": rows_us, "union_tc_us": tc_us, "union_build_us": statistics.median(build),
+            "rows_over_union_tc": rows_us / tc_us}
+
+
 def hybrid_leg(tw, flush, stream, reps: int = 5):
     """The skewed sweep workloads (8192 tokens, d_model 4096, d_ff 16384, x rows
     scaled by LogNormal(0, 1), gate biases for nominal 90 / 99 / 99.9 %
@@ -565,6 +605,7 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
         ms_tw = timed(lambda: tw.twell_ffn_fwd(x, Wu, None, b, Wd, T, buf, y, ws, st))
         slots, nnz = buf.slots(), int(buf.nnz.sum().item())
         del ws
+        down = down_variants(tw, buf, Wd, y, st, flush, stream)
         wsb = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, M * F), dtype=torch.uint8,
                           device="cuda")
         ms_tw_b = timed(lambda: tw.twell_ffn_bwd(x, Wu, Wd, buf, dy, l1, dx, dWu, dWd, db, wsb, st), n=2)
@@ -589,7 +630,8 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
                      "dense_step_estimate_ms": 3 * ms_d,
                      "twell_MB": slots * 6 / 1e6, "hybrid_MB": (ell_slots * 6 + n_ov * F * 2) / 1e6,
                      "overflow_rows": n_ov, "hybrid_vs_twell": ms_tw / ms_h, "hybrid_vs_dense": ms_d / ms_h,
-                     "hybrid_step_vs_twell_step": (ms_tw + ms_tw_b) / (ms_h + ms_h_b)}
+                     "hybrid_step_vs_twell_step": (ms_tw + ms_tw_b) / (ms_h + ms_h_b),
+                     "down_projection": down}
     return out
 
 
@@ -638,6 +680,7 @@ def training_leg(tw, flush, stream, reps: int = 5):
     bwd = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     nnz = int(buf.nnz.sum().item())
     del ws_b, dWu, dWd
+    down = down_variants(tw, buf, Wd, y, st, flush, stream)
     WdT = Wd.view(F, d).t().contiguous()
     hd = torch.empty(M, F, dtype=torch.int16, device="cuda")
     dts = []
@@ -654,8 +697,17 @@ def training_leg(tw, flush, stream, reps: int = 5):
     return {"workload": f"M={M}, d_model={d}, d_ff={F}, T={T}, bias={c['bias']}, l1={c['l1']}",
             "density": nnz / (M * F), "fwd_ms": fwd, "bwd_ms": bwd, "step_ms": fwd + bwd,
             "tokens_per_s": M / ((fwd + bwd) / 1000.0), "dense_fwd_ms": dense_fwd,
-            "dense_step_estimate_ms": 3 * dense_fwd,
+            "dense_step_estimate_ms": 3 * dense_fwd, "down_projection": down,
             "dense_step_note": "3 x the measured dense forward: a dense backward runs each forward GEMM shape twice"}
+
+
+EXTRA_LEGS = ("e2e", "dense", "energy", "down", "decode", "hybrid", "training")
+
+
+def leg_on(args, name: str) -> bool:
+    if args.no_extras:
+        return False
+    return args.legs == "all" or name in args.legs.split(",")
 
 
 def run_ours(args, rank: int, world: int, local_rank: int):
@@ -765,7 +817,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # ---- end to end through the public API with host buffers
     e2e = None
-    if not args.no_extras:
+    if leg_on(args, "e2e"):
         xh = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).pin_memory()
         dyh = torch.from_numpy(np.ascontiguousarray(inp.dy).view(np.int16)).pin_memory()
         yh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
@@ -795,7 +847,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     WdT = L.Wd.view(inp.F, inp.d).t().contiguous()
     hd = torch.empty(inp.M, inp.F, dtype=torch.int16, device="cuda")
     dts = []
-    for i in range(0 if args.no_extras else 13):
+    for i in range(13 if leg_on(args, "dense") else 0):
         flush.fill_(i & 0xff)
         a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -807,7 +859,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # ---- energy per token and memory, sparse against dense (forward; and the sparse training step)
     energy, memory = None, None
-    if not args.no_extras:
+    if leg_on(args, "energy"):
         energy = energy_leg(tw, local_rank, {
             "twell_fwd": lambda: tw.twell_ffn_fwd(L.x, L.Wu, None, L.b, L.Wd, inp.T, L.buf, L.y, L.ws_f, L.st),
             "dense_fwd": lambda: tw.twell_dense_ffn_fwd(L.x, L.Wu, L.b, WdT, hd, L.y, L.st),
@@ -823,9 +875,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "backward_workspace_MB": {"twell_at_actual_slots": tw.twell_workspace_bytes(
                 tw.OP_FFN_BWD, inp.M, inp.d, inp.F, inp.T, slots) / 1e6},
         }
-    decode = None if args.no_extras else decode_leg(tw, peaks, flush, stream)
-    hybrid = None if args.no_extras else hybrid_leg(tw, flush, stream)
-    training = None if args.no_extras else training_leg(tw, flush, stream)
+    union = down_variants(tw, L.buf, L.Wd, L.y, L.st, flush, stream, reps=10) if leg_on(args, "down") else None
+    decode = decode_leg(tw, peaks, flush, stream) if leg_on(args, "decode") else None
+    hybrid = hybrid_leg(tw, flush, stream) if leg_on(args, "hybrid") else None
+    training = training_leg(tw, flush, stream) if leg_on(args, "training") else None
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.no_extras:
@@ -853,6 +906,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "stages": stages,
         "kernels": kernels,
         "dense_tcgen05_fwd_ms": dense_ms,
+        "down_projection": union,
         "hybrid": hybrid,
         "training": training,
         "energy": energy,
@@ -872,6 +926,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e, dense and CPU legs (profiling runs)")
+    ap.add_argument("--legs", default="all",
+                    help="comma list of the extra legs to run: e2e, dense, energy, down, decode, hybrid, training "
+                         "(default all; --no-extras runs none)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))

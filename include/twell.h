@@ -140,6 +140,24 @@ twell_status twell_spmm_down(const twell_buf* h, const uint16_t* W_down, int d,
                              uint16_t* y, int32_t* status, void* stream);
 
 /*
+ * twell_spmm_down_tc — the same product y = h W_down on the tensor cores
+ * (Resumo Técnico §2, "Kernels de Inferência": only the active neurons are
+ * visited and the tensor cores do the multiplication). For each group of 128
+ * consecutive tokens, U is the ascending union of their active units; then
+ * y[group] = h[group, U] W_down[U, :] runs as one tcgen05 GEMM with K = |U|
+ * (A built in shared memory from the TwELL, B the gathered rows of W_down).
+ * Same arguments, result and error behaviour as twell_spmm_down, plus:
+ *   ws        device workspace of at least
+ *             twell_spmm_down_tc_workspace_bytes(h->M, h->F, h->cap_slots)
+ *             bytes, 256-byte aligned; contents are scratch
+ * h->F must be a multiple of 8 and at most 65536 (TWELL_ERR_UNSUPPORTED).
+ * y equals twell_spmm_down's up to fp32 summation order.
+ */
+size_t twell_spmm_down_tc_workspace_bytes(int M, int F, int64_t cap_slots);
+twell_status twell_spmm_down_tc(const twell_buf* h, const uint16_t* W_down, int d, uint16_t* y,
+                                void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
+/*
  * twell_ffn_fwd — the layer's forward pass.
  *   ReLU  (W_gate == NULL): h = relu(x W_up^T + b), packed into TwELL inside the
  *          tcgen05 up-projection's epilogue (Resumo Técnico §2: TwELL materialised
@@ -309,10 +327,12 @@ twell_status twell_ffn_fwd_static_ws(const uint16_t* x, const uint16_t* W_up, co
  *   7 gated decode tail (M <= 64: layout, gated up products and, in
  *     twell_ffn_fwd, the down-projection, in one launch)
  *   8 dense GEMM of the hybrid format's overflow rows (twell_hybrid_spmm_down)
+ *   9 union down-projection on the tensor cores (twell_spmm_down_tc, both kernels)
+ *  10 its first kernel alone (the groups' unions and entry buckets)
  */
 enum { TWELL_SITE_NONE = 0, TWELL_SITE_UP_GEMM = 1, TWELL_SITE_SPMM_DOWN = 2, TWELL_SITE_SDDMM = 3,
        TWELL_SITE_DX = 4, TWELL_SITE_CSC = 5, TWELL_SITE_WGRAD = 6, TWELL_SITE_DECODE_TAIL = 7,
-       TWELL_SITE_OVERFLOW_GEMM = 8 };
+       TWELL_SITE_OVERFLOW_GEMM = 8, TWELL_SITE_SPMM_UNION = 9, TWELL_SITE_UNION_BUILD = 10 };
 twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end);
 
 /*

@@ -50,6 +50,12 @@ def test_slot_bound_and_workspace_sizes(lib):
     bwd_big = tw.twell_workspace_bytes(tw.OP_FFN_BWD, 4096, 2048, 8192, 128, 1_000_000)
     assert bwd_big - bwd_small >= 3 * 4 * 990_000 - 3 * 256  # dpre, row and slot per stored entry
     assert tw.twell_workspace_bytes(tw.OP_FFN_FWD, 0, 2048, 8192, 128) == 0
+    # union down-projection: per group a list of F unit ids, plus one word per stored entry
+    u_small = tw.twell_spmm_down_tc_workspace_bytes(4096, 8192, 10_000)
+    u_big = tw.twell_spmm_down_tc_workspace_bytes(4096, 8192, 1_000_000)
+    assert u_small >= 32 * 8192 * 4 and u_big - u_small >= 4 * 990_000 - 256
+    assert tw.twell_spmm_down_tc_workspace_bytes(4096, 65544, 10) == 0
+    assert tw.twell_spmm_down_tc_workspace_bytes(4096, 100, 10) == 0  # F % 8 != 0
 
 
 def test_host_argument_errors_need_no_gpu(lib):
@@ -70,7 +76,12 @@ def test_host_argument_errors_need_no_gpu(lib):
     fake = ctypes.c_void_p(256)  # never dereferenced: d % 8 != 0 is rejected first
     rc = lib.twell_gather_probe(fake, 8192, 2044, fake, 4096, 82, fake, None)
     assert rc == 1
-    assert lib.twell_set_kernel_timer(9, None, None) == 1  # no such call site
+    assert lib.twell_set_kernel_timer(11, None, None) == 1  # no such call site
+    rc = lib.twell_spmm_down_tc(None, None, 128, None, None, 0, None, None)
+    assert rc == 1
+    big = tw._TwellBuf(64, 65544, 16, 4, 0, fake, fake, fake, None, None)  # F above the union kernel's limit
+    rc = lib.twell_spmm_down_tc(ctypes.byref(big), fake, 128, fake, fake, 1 << 20, fake, None)
+    assert rc == 2  # TWELL_ERR_UNSUPPORTED
     assert lib.twell_wait_selftest(2, fake, fake, None) == 1  # no such wait
     assert lib.twell_wait_selftest(0, None, None, None) == 1
 
