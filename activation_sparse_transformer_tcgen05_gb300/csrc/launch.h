@@ -91,8 +91,12 @@ struct CscWork {
     float* cdpre;               // [cap] its dpre
 };
 void csc_plan(int M, int F, int* row_blocks, int* rows_per_block);
-// Column lists of the stored entries with their row, h and dpre (dpre: [slots], by slot).
-cudaError_t launch_csc(const TwellView& tw, const CscWork& w, const float* dpre, int32_t* status, cudaStream_t s);
+// Column lists of the stored entries: masks, per-(block, column) starts and
+// column pointers (the TwELL indices only) ...
+cudaError_t launch_csc_lists(const TwellView& tw, const CscWork& w, int32_t* status, cudaStream_t s);
+// ... then every entry's row, h and dpre at its place (dpre: [slots], by slot).
+cudaError_t launch_csc_scatter(const TwellView& tw, const CscWork& w, const float* dpre, int32_t* status,
+                               cudaStream_t s);
 // dW_down[j] = sum h dy[r], dW_up[j] = sum dpre x[r], db[j] = sum dpre over column j.
 cudaError_t launch_wgrad(const TwellView& tw, const CscWork& w, const float* dpre, const uint16_t* x,
                          const uint16_t* dy, int d, float* dW_up, float* dW_down, float* db, int32_t* status,

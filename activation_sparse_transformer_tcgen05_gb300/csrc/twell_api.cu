@@ -27,6 +27,37 @@ int sm_count_current()
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A second stream and two events per (host thread, device), created on first
+// use and kept until the process ends: the backward forks independent kernels
+// onto it. Null if they cannot be created (the kernels then run in order).
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    int state = 0;  // 0 not tried, 1 ready, -1 unavailable
+};
+
+SideStream* side_stream(cudaStream_t caller)
+{
+    thread_local SideStream per_device[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    SideStream& ss = per_device[dev];
+    if (ss.state == 0) {
+        // never create resources while the caller's stream is being captured
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        const bool ok = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) == cudaSuccess &&
+                        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) == cudaSuccess &&
+                        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) (void)cudaGetLastError();
+        ss.state = ok ? 1 : -1;
+    }
+    return ss.state == 1 ? &ss : nullptr;
+}
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace carving: consecutive 256-byte-aligned regions.
@@ -514,15 +545,31 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
     const TwellView tw = view_of(h);
     BwdWs w;
     carve_bwd(ws, M, F, h->cap_slots, &w);
+    // The column lists' first kernels read only the TwELL indices: they run on
+    // a side stream under the SDDMM (fork and join by events, which stream
+    // capture also records); without a side stream they run first on s.
+    SideStream* side = side_stream(s);
+    cudaError_t e = cudaSuccess;
+    if (side) {
+        e = cudaEventRecord(side->fork, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+        timer_begin(TWELL_SITE_CSC, side->s);
+        if (e == cudaSuccess) e = launch_csc_lists(tw, w.csc, status, side->s);
+        timer_end(TWELL_SITE_CSC, side->s);
+        if (e == cudaSuccess) e = cudaEventRecord(side->join, side->s);
+    } else {
+        timer_begin(TWELL_SITE_CSC, s);
+        e = launch_csc_lists(tw, w.csc, status, s);
+        timer_end(TWELL_SITE_CSC, s);
+    }
     timer_begin(TWELL_SITE_SDDMM, s);
-    cudaError_t e = launch_sddmm(tw, dy, W_down, d, l1_coef, w.dpre, status, s);
+    if (e == cudaSuccess) e = launch_sddmm(tw, dy, W_down, d, l1_coef, w.dpre, status, s);
     timer_end(TWELL_SITE_SDDMM, s);
     timer_begin(TWELL_SITE_DX, s);
     if (e == cudaSuccess) e = launch_spmm_rows(tw, w.dpre, W_up, d, dx, status, s);
     timer_end(TWELL_SITE_DX, s);
-    timer_begin(TWELL_SITE_CSC, s);
-    if (e == cudaSuccess) e = launch_csc(tw, w.csc, w.dpre, status, s);
-    timer_end(TWELL_SITE_CSC, s);
+    if (e == cudaSuccess && side) e = cudaStreamWaitEvent(s, side->join, 0);
+    if (e == cudaSuccess) e = launch_csc_scatter(tw, w.csc, w.dpre, status, s);
     timer_begin(TWELL_SITE_WGRAD, s);
     if (e == cudaSuccess) e = launch_wgrad(tw, w.csc, w.dpre, x, dy, d, dW_up, dW_down, db, status, s);
     timer_end(TWELL_SITE_WGRAD, s);

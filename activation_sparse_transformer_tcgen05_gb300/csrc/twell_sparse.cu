@@ -1449,7 +1449,7 @@ void csc_plan(int M, int F, int* row_blocks, int* rows_per_block)
     *row_blocks = (M + kCscRows - 1) / kCscRows;
 }
 
-cudaError_t launch_csc(const TwellView& tw, const CscWork& w, const float* dpre, int32_t* status, cudaStream_t s)
+cudaError_t launch_csc_lists(const TwellView& tw, const CscWork& w, int32_t* status, cudaStream_t s)
 {
     // split the columns so that the mask pass has at least two blocks per SM
     int splits = (2 * 152 + w.row_blocks - 1) / w.row_blocks;
@@ -1462,10 +1462,17 @@ cudaError_t launch_csc(const TwellView& tw, const CscWork& w, const float* dpre,
     const size_t smem = (size_t)col_range * sizeof(unsigned long long);
     cudaError_t e = cudaFuncSetAttribute(k_csc_mask, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    count_launches(4);
+    count_launches(3);
     k_csc_mask<<<dim3(w.row_blocks, ny), 256, smem, s>>>(tw, col_range, w.masks, status);
     k_csc_colscan<<<(tw.F + 31) / 32, 1024, 0, s>>>(w.masks, w.row_blocks, tw.F, w.start, w.colcnt, status);
     k_scan_i32<<<1, 1024, 0, s>>>(w.colcnt, tw.F, w.colptr, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_csc_scatter(const TwellView& tw, const CscWork& w, const float* dpre, int32_t* status,
+                               cudaStream_t s)
+{
+    count_launches(1);
     k_csc_scatter<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, w.masks, w.start, w.colptr, dpre, w.crow,
                                                                w.cval, w.cdpre, status);
     return cudaGetLastError();

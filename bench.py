@@ -237,6 +237,10 @@ class Layer:
 
 
 SITES = {1: "up_gemm", 2: "spmm_down", 3: "sddmm", 4: "dx", 5: "csc", 6: "wgrad"}
+# Call sites whose kernels run on the library's side stream, concurrently with
+# another site's: their event time spans that overlap, so they never count as
+# the dominant kernel.
+CONCURRENT_SITES = {5: "sddmm"}
 
 
 class PowerSampler:
@@ -754,7 +758,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         tw.twell_set_kernel_timer(0)
         torch.cuda.synchronize()
         site_us[site] = statistics.mean(a.elapsed_time(b2) for a, b2 in evs[1:]) * 1000.0
-    dom_site = max(site_us, key=site_us.get)
+    dom_site = max((k for k in site_us if k not in CONCURRENT_SITES), key=site_us.get)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -814,6 +818,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         gk = gather_roofline(k, v, nnz, inp.d, ceiling)
         if gk:
             kernels[SITES[k]]["l2_gather_frac"] = gk["frac"]
+        if k in CONCURRENT_SITES:
+            kernels[SITES[k]]["concurrent_with"] = CONCURRENT_SITES[k]
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -824,17 +830,40 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         dxh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
         ke = max(3, min(args.steps, 50))
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
+        # Each step copies x in, runs the forward, copies y out, runs the
+        # backward and copies dx out; dy (needed only by the backward) comes in
+        # and y goes out on a copy stream while the compute stream works.
+        cstream = torch.cuda.Stream()
+        bwd_done = torch.cuda.Event()
+        bwd_done.record(stream)
         for i in range(ke + 3):
             flush.fill_(i & 0xff)
             e = evs[i - 3] if i >= 3 else None
             if e:
                 e[0].record(stream)
+            start = torch.cuda.Event()
+            start.record(stream)
             L.x.copy_(xh, non_blocking=True)
-            L.dy.copy_(dyh, non_blocking=True)
+            cstream.wait_event(start)
+            cstream.wait_event(bwd_done)  # the previous backward has read dy
+            with torch.cuda.stream(cstream):
+                L.dy.copy_(dyh, non_blocking=True)
+            dy_in = torch.cuda.Event()
+            dy_in.record(cstream)
             tw.twell_ffn_fwd(L.x, L.Wu, None, L.b, L.Wd, inp.T, L.buf, L.y, L.ws_f, L.st)
+            fwd_done = torch.cuda.Event()
+            fwd_done.record(stream)
+            cstream.wait_event(fwd_done)
+            with torch.cuda.stream(cstream):
+                yh.copy_(L.y, non_blocking=True)
+            y_out = torch.cuda.Event()
+            y_out.record(cstream)
+            stream.wait_event(dy_in)
             L.bwd()
-            yh.copy_(L.y, non_blocking=True)
+            bwd_done = torch.cuda.Event()
+            bwd_done.record(stream)
             dxh.copy_(L.dx, non_blocking=True)
+            stream.wait_event(y_out)  # the step ends when y has reached the host too
             if e:
                 e[1].record(stream)
         torch.cuda.synchronize()

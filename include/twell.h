@@ -26,11 +26,14 @@
  *     "host". bf16 tensors are passed as uint16_t bit arrays; all matrices are
  *     row-major and densely packed (row stride = column count) unless a leading
  *     dimension is given. Weights are [F, d]: one row per hidden unit.
- *   - The caller owns and allocates every buffer. The library never allocates,
- *     frees or synchronises (twell_check is the one call that synchronises);
- *     each call only enqueues work on `stream` (a cudaStream_t passed as void*,
- *     NULL = the legacy default stream) and returns. Buffers must stay alive
- *     until that work has finished.
+ *   - The caller owns and allocates every buffer. The library never allocates
+ *     memory, frees or synchronises (twell_check is the one call that
+ *     synchronises); each call only enqueues work on `stream` (a cudaStream_t
+ *     passed as void*, NULL = the legacy default stream) and returns. Buffers
+ *     must stay alive until that work has finished. twell_ffn_bwd forks part
+ *     of its work onto a library stream and joins it back through events: one
+ *     stream and two events per host thread and device, created by the first
+ *     call that is not being stream-captured and kept until the process ends.
  *   - Host-side argument errors are returned at once and nothing is enqueued.
  *     Errors found on the device (capacity, bounded-wait timeout) are written
  *     to `*status`, a caller-owned device int32 that the caller sets to 0
@@ -265,6 +268,8 @@ twell_status twell_hybrid_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const
  *   M, d, F, T, h->cap_slots) bytes, 256-byte aligned. Limits of this build:
  *   d <= 4096, h->cap_slots < 2^31 (else TWELL_ERR_UNSUPPORTED).
  * The reduction order of every sum is fixed (no floating-point atomics).
+ * The column lists' index-only kernels run on the library's side stream while
+ * the SDDMM runs on `stream`; the call's work is complete when `stream`'s is.
  */
 twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down,
                            const twell_buf* h, const uint16_t* dy, int d, float l1_coef,
@@ -322,7 +327,8 @@ twell_status twell_ffn_fwd_static_ws(const uint16_t* x, const uint16_t* W_up, co
  *   1 up-projection GEMM (twell_up_pack / twell_ffn_fwd)
  *   2 sparse down-projection (twell_spmm_down / twell_ffn_fwd)
  *   3 backward SDDMM            4 backward dx
- *   5 backward column lists (first to last of its kernels)
+ *   5 backward column lists: the kernels that read only the TwELL indices
+ *     (on the library's side stream, concurrently with the SDDMM)
  *   6 backward weight gradients
  *   7 gated decode tail (M <= 64: layout, gated up products and, in
  *     twell_ffn_fwd, the down-projection, in one launch)

@@ -451,3 +451,41 @@ def test_fwd_staging_overflow_is_reported():
     inp = syn.ffn_inputs(300, 128, 1024, 32, 0.0, seed=9)
     _, _, st = _fwd_with_stage_cap(inp, 32)
     assert tw.twell_check(st) == 4  # TWELL_ERR_CAPACITY
+
+
+def test_bwd_replayed_from_a_cuda_graph_matches_eager():
+    """The backward forks its index-only column-list kernels onto a side stream
+    and joins them back by events; captured in a CUDA graph and replayed it must
+    give the eager result bit for bit (and the oracle's within tolerance)."""
+    M, d, F, T = 200, 264, 520, 32
+    inp = syn.ffn_inputs(M, d, F, T, -1.5, seed=9, with_dy=True)
+    fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, want_y=False)
+    ref_tw = oracle.twell_pack(fw["h"], T)
+    eager = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, 1e-3)  # also creates the side stream
+    buf = twell_to_device(ref_tw)
+    x, Wu, Wd, dy = dev_bf16(inp.x), dev_bf16(inp.W_up), dev_bf16(inp.W_down), dev_bf16(inp.dy)
+    dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    db = torch.empty(F, dtype=torch.float32, device="cuda")
+    ws = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, buf.cap_slots), dtype=torch.uint8,
+                     device="cuda")
+    st = status_tensor()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tw.twell_ffn_bwd(x, Wu, Wd, buf, dy, 1e-3, dx, dWu, dWd, db, ws, st)
+    for _ in range(2):
+        dx.zero_(), dWu.zero_(), dWd.zero_(), db.zero_()
+        g.replay()
+        _status_ok(st)
+        got = (bf16_f64(host_bf16_bits(dx)), dWu.cpu().numpy(), dWd.cpu().numpy(), db.cpu().numpy())
+        for u, v in zip(got, eager):
+            np.testing.assert_array_equal(u, v)
+    X, WU, WD, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, fw["h"], inp.dy))
+    _, dx_ref = oracle.ffn_bwd_rows(X, WU, WD, H, DY, 1e-3)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, WU, WD, H, DY, 1e-3)
+    assert_close_rms(got[0], dx_ref, what="dx", bf16_out=True)
+    assert_close_rms(got[1], gu, what="dW_up")
+    assert_close_rms(got[2], gd, what="dW_down")
+    assert_close_rms(got[3], gb, what="db")
