@@ -330,11 +330,11 @@ def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:
 # the SHA-256 of the source file it was built from: once that file changes the
 # figure no longer describes the kernel and the site reports traffic null.
 NCU_TRAFFIC = {
-    1: ("twell_gemm.cu", "26dfe7157735f1512e423b5748429ec2141ba9124d9bd14beb4892b356f8ab92", 53.190912e6),
-    2: ("twell_sparse.cu", "f46042fdf24ecd8ce915e7c89d019d39a9e6af6e77a3f317713719cfa19ecb30", 37.771264e6),
-    3: ("twell_sparse.cu", "f46042fdf24ecd8ce915e7c89d019d39a9e6af6e77a3f317713719cfa19ecb30", 52.516608e6),
-    4: ("twell_sparse.cu", "f46042fdf24ecd8ce915e7c89d019d39a9e6af6e77a3f317713719cfa19ecb30", 38.86336e6),
-    6: ("twell_sparse.cu", "f46042fdf24ecd8ce915e7c89d019d39a9e6af6e77a3f317713719cfa19ecb30", 132.71808e6),
+    1: ("twell_gemm.cu", "26dfe7157735f1512e423b5748429ec2141ba9124d9bd14beb4892b356f8ab92", 52.946176e6),
+    2: ("twell_sparse.cu", "4b7c58e6176bed50c54b847161a48419ff7d3065e044164f018d213fcae6c6bf", 37.770496e6),
+    3: ("twell_sparse.cu", "4b7c58e6176bed50c54b847161a48419ff7d3065e044164f018d213fcae6c6bf", 52.641792e6),
+    4: ("twell_sparse.cu", "4b7c58e6176bed50c54b847161a48419ff7d3065e044164f018d213fcae6c6bf", 38.832384e6),
+    6: ("twell_sparse.cu", "4b7c58e6176bed50c54b847161a48419ff7d3065e044164f018d213fcae6c6bf", 133.058816e6),
 }
 
 
