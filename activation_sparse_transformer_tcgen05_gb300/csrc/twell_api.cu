@@ -288,6 +288,13 @@ twell_status twell_spmm_down_tc(const twell_buf* h, const uint16_t* W_down, int 
     twell_status st = check_buf(h, h->M, h->F, h->T);
     if (st != TWELL_OK) return st;
     if (h->F > kUnionMaxF) return TWELL_ERR_UNSUPPORTED;
+    {
+        int dev = 0, optin = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return TWELL_ERR_CUDA;
+        if (union_smem_bytes(h->F) > (size_t)optin) return TWELL_ERR_UNSUPPORTED;
+    }
     if (!ws) return TWELL_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;
     if (ws_bytes < carve_union(nullptr, h->M, h->F, h->cap_slots, nullptr)) return TWELL_ERR_WORKSPACE;

@@ -558,8 +558,10 @@ cudaError_t run_union(const TwellView& tw, const uint16_t* W, int d, const Union
 
 // Tile shapes: 128 x 256 (B ring 5 x 32 KB, bucket ring 4 x 4 KB, A ring 2 x 16 KB)
 // and, for d <= 128, 128 x 128 (B ring 8 x 16 KB, bucket ring 4 x 4 KB, A ring 3 x 16 KB).
-using Wide = ULayout<256, 5, 4, 2, 2>;
-using Narrow = ULayout<128, 8, 4, 2, 3>;
+#define TWELL_UNION_WIDE 256, 5, 4, 2, 2
+#define TWELL_UNION_NARROW 128, 8, 4, 2, 3
+using Wide = ULayout<TWELL_UNION_WIDE>;
+using Narrow = ULayout<TWELL_UNION_NARROW>;
 
 }  // namespace
 
@@ -587,8 +589,8 @@ cudaError_t launch_union_build(const TwellView& tw, const UnionWork& w, int32_t*
 cudaError_t launch_spmm_union(const TwellView& tw, const uint16_t* W, int d, const UnionWork& w, uint16_t* y,
                               int32_t* status, cudaStream_t s)
 {
-    if (d <= 128) return run_union<128, 8, 4, 2, 3>(tw, W, d, w, y, status, s);
-    return run_union<256, 5, 4, 2, 2>(tw, W, d, w, y, status, s);
+    if (d <= 128) return run_union<TWELL_UNION_NARROW>(tw, W, d, w, y, status, s);
+    return run_union<TWELL_UNION_WIDE>(tw, W, d, w, y, status, s);
 }
 
 }  // namespace twell

@@ -2,7 +2,8 @@
 128-token group unions, against the CPU oracle's y = h W_down (2e-2 * rms(ref),
 bf16 output). Shapes cover: d below and above one 256-column block, ragged
 groups, F not a multiple of the 64-deep k-block, T not dividing the group,
-buckets larger than the staged part (global fallback), empty and full h."""
+buckets larger than the staged part (global fallback), empty and full h, and
+the largest d_ff the kernel takes."""
 import numpy as np
 import pytest
 import torch
@@ -47,6 +48,8 @@ def _run_tc(buf, W, M, d, guard=False):
     (200, 4096, 256, 128, 0.9, 5),    # nearly dense: U = F, large buckets
     (40, 256, 128, 16, 0.0, 6),       # nothing active: y = 0
     (33, 64, 72, 8, 1.0, 7),          # everything active
+    (130, 65536, 128, 64, 0.002, 8),  # the largest d_ff (shared memory of both tile shapes at their limit)
+    (130, 65536, 264, 64, 0.002, 9),
 ])
 def test_spmm_down_tc_matches_oracle(M, F, d, T, density, seed):
     h = syn.sparse_hidden(M, F, density, seed=seed)
