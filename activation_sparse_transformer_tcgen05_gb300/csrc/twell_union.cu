@@ -30,14 +30,16 @@
 //                   copies themselves (cp.async.mbarrier.arrive.noinc). Waiting
 //                   for copy groups instead and arriving plainly was slower:
 //                   it ties the loader to copies issued a few k-blocks back.
-//     warps 0-3     builders, then epilogue: per k-block, once its copies have
-//                   landed, zero the A slot (token row per thread, K-major,
-//                   128-byte swizzle), scatter the bucket into it, fence the
-//                   generic-proxy writes for the tensor cores and arrive on
-//                   the slot's full barrier. They hold no copies in flight, so
-//                   the fence has nothing to wait for. After the loop each
-//                   thread reads its accumulator row from TMEM, writes bf16 y.
-//     warp 12       TMEM owner and MMA issuer (M = 128 tokens, N = BN, K = 16).
+//     warps 0-3     builders, then epilogue: per k-block, once its bucket has
+//                   landed (its W rows may still be in flight), zero the A
+//                   slot (token row per thread, K-major, 128-byte swizzle),
+//                   scatter the bucket into it, fence the generic-proxy writes
+//                   for the tensor cores and arrive on the slot's full
+//                   barrier. After the loop each thread reads its accumulator
+//                   row from TMEM and writes bf16 y.
+//     warp 12       TMEM owner and MMA issuer (M = 128 tokens, N = BN, K = 16):
+//                   per k-block it waits for the A tile and for the landed W
+//                   rows, and fences the latter for the tensor cores.
 // Measured limit: the loaders' cp.async gathers. Issuing a k-block's 32 KB
 // takes ~0.6 us per SM whatever the ring depths (about 53 GB/s per SM), where
 // the row gather of k_spmm_rows, with plain loads from many warps, reaches
@@ -53,7 +55,6 @@ namespace {
 
 constexpr int UG = 128;        // tokens per group (MMA M)
 constexpr int UBK = 64;        // units per k-block (one 128-byte swizzle row of bf16)
-constexpr int kProducers = 128;
 constexpr int kUnionThreads = 1024;
 constexpr int kLoaders = 256;                // loader threads (warps 4 .. 4 + kLoaders / 32 - 1)
 constexpr int kMmaWarp = 4 + kLoaders / 32;  // TMEM owner and MMA issuer
@@ -68,8 +69,8 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (tensor core) reads of them.
+// Orders the generic-proxy shared-memory writes this thread made, or has seen
+// complete through a barrier, before its later async-proxy (tensor core) reads.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // First TwELL slot of row r.
