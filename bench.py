@@ -708,6 +708,11 @@ def training_leg(tw, flush, stream, reps: int = 5):
 EXTRA_LEGS = ("e2e", "dense", "energy", "down", "decode", "hybrid", "training")
 
 
+def dominant_site(site_us: dict) -> int:
+    """The call site with the longest time among those that run alone."""
+    return max((k for k in site_us if k not in CONCURRENT_SITES), key=site_us.get)
+
+
 def leg_on(args, name: str) -> bool:
     if args.no_extras:
         return False
@@ -758,7 +763,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         tw.twell_set_kernel_timer(0)
         torch.cuda.synchronize()
         site_us[site] = statistics.mean(a.elapsed_time(b2) for a, b2 in evs[1:]) * 1000.0
-    dom_site = max((k for k in site_us if k not in CONCURRENT_SITES), key=site_us.get)
+    dom_site = dominant_site(site_us)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]

@@ -66,3 +66,17 @@ def test_reference_arm_runs_on_rank_zero_only():
     with contextlib.redirect_stdout(out):
         bench.run_reference(types.SimpleNamespace(steps=1, warmup=3), rank=1, world=2)
     assert out.getvalue() == ""
+
+
+def test_extra_legs_and_dominant_site_selection():
+    sys.path.insert(0, ROOT)
+    import bench
+    args = types.SimpleNamespace(no_extras=False, legs="all")
+    assert all(bench.leg_on(args, leg) for leg in bench.EXTRA_LEGS)
+    args.legs = "down,decode"
+    assert bench.leg_on(args, "down") and bench.leg_on(args, "decode") and not bench.leg_on(args, "hybrid")
+    args.no_extras = True
+    assert not any(bench.leg_on(args, leg) for leg in bench.EXTRA_LEGS)
+    # a site whose kernels overlap another site's (its events span both) is never the dominant one
+    times = {1: 83.0, 2: 99.0, 3: 113.0, 4: 117.0, 5: 232.0, 6: 198.0}
+    assert 5 in bench.CONCURRENT_SITES and bench.dominant_site(times) == 6
