@@ -153,8 +153,11 @@ twell_status twell_spmm_down(const twell_buf* h, const uint16_t* W_down, int d,
  *   ws        device workspace of at least
  *             twell_spmm_down_tc_workspace_bytes(h->M, h->F, h->cap_slots)
  *             bytes, 256-byte aligned; contents are scratch
- * h->F must be a multiple of 8 and at most 65536 (TWELL_ERR_UNSUPPORTED).
- * y equals twell_spmm_down's up to fp32 summation order.
+ * h->F must be a multiple of 8 and at most 65536, and the device must offer
+ * the kernel's shared memory (about 227 KB per block; else
+ * TWELL_ERR_UNSUPPORTED). y equals twell_spmm_down's up to fp32 summation
+ * order. Launches two kernels: the groups' unions and entry buckets, then the
+ * GEMM.
  */
 size_t twell_spmm_down_tc_workspace_bytes(int M, int F, int64_t cap_slots);
 twell_status twell_spmm_down_tc(const twell_buf* h, const uint16_t* W_down, int d, uint16_t* y,
