@@ -33,7 +33,9 @@
  *     must stay alive until that work has finished. twell_ffn_bwd forks part
  *     of its work onto a library stream and joins it back through events: one
  *     stream and two events per host thread and device, created by the first
- *     call that is not being stream-captured and kept until the process ends.
+ *     call that is not being stream-captured and kept until the process ends
+ *     (cudaDeviceReset invalidates them; later backward calls on that thread
+ *     and device then return TWELL_ERR_CUDA).
  *   - Host-side argument errors are returned at once and nothing is enqueued.
  *     Errors found on the device (capacity, bounded-wait timeout) are written
  *     to `*status`, a caller-owned device int32 that the caller sets to 0
