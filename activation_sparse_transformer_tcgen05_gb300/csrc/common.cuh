@@ -54,6 +54,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
 }
 
+// ------------------------------------------------------------ warp sums --
+
+// After this, lane u holds the sum over all 32 lanes of v[u] (in v[0]): a
+// butterfly where each step keeps the half of the values that belongs to the
+// lane's side and adds the partner's copy of that half (31 shuffles in all).
+__device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -173,7 +192,8 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (both
 // K-major), fp32 D, shape M x N (M = 64 or 128 on one CTA, 256 over a CTA
-// pair with cta_group::2; N a multiple of 16 up to 256).
+// pair with cta_group::2; N a multiple of 16 up to 256). An MN-major operand
+// sets its transpose bit: kIdescAMn for A, kIdescBMn for B.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
 {
     return (1u << 4)                          // D format: f32
@@ -182,6 +202,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
+
+constexpr uint32_t kIdescAMn = 1u << 15;
+constexpr uint32_t kIdescBMn = 1u << 16;
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
 // with 128-byte swizzle: rows of 64 bf16 (128 B), 8-row core groups 1024 B
@@ -195,6 +218,22 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr)
     d |= (uint64_t)(1024u >> 4) << 32;            // stride byte offset: 8 rows x 128 B
     d |= (uint64_t)1u << 46;                      // descriptor version (tcgen05)
     d |= (uint64_t)2u << 61;                      // swizzle mode: 128 B
+    return d;
+}
+
+// Shared-memory descriptor of an MN-major operand written with the 128-byte
+// swizzle: 64 contiguous elements (128 B) along MN per row, 8 rows along K
+// per 1024-byte atom; `mn_stride` bytes between 64-element blocks along MN
+// (leading byte offset), 1024 bytes between 8-row groups along K (stride
+// byte offset).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t mn_stride)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
     return d;
 }
 

@@ -72,9 +72,12 @@ cudaError_t launch_layout_fill_small_relu(const uint32_t* stage, const int32_t* 
 // or an fp32 array indexed by slot.
 cudaError_t launch_spmm_rows(const TwellView& tw, const float* vals_f32, const uint16_t* W, int d,
                              uint16_t* y, int32_t* status, cudaStream_t s);
-// dpre[slot] = dy[r] . W[idx] + l1 on stored slots, 0 on padding.
+// dpre[slot] = dy[r] . W[idx] + l1 on stored slots, 0 on padding. The dot
+// products run over column slices of up to 1024 columns; part holds
+// sddmm_slices(d) * tw.cap floats of per-slice sums (workspace).
+int sddmm_slices(int d);
 cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float l1,
-                         float* dpre, int32_t* status, cudaStream_t s);
+                         float* dpre, float* part, int32_t* status, cudaStream_t s);
 // Gated: val[slot] = bf16(relu(g) * (x[r] . W_up[idx])) on stored slots.
 cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16_t* W_up, int d,
                             const float* gval, int32_t* status, cudaStream_t s);
@@ -115,7 +118,9 @@ cudaError_t launch_decode_tail(const uint2* gstage, const int32_t* stage_cnt, in
                                uint16_t* y, int32_t* counter, int32_t* status, cudaStream_t s);
 
 struct GemmArgs {
-    int rowsA, rowsB, K;   // A [rowsA, K], B [rowsB, K], both bf16 K-major
+    int rowsA, rowsB, K;   // A [rowsA, K], B [rowsB, K] bf16, K-major unless a_mn / b_mn
+    int a_mn, b_mn;        // DENSE only: the operand is stored MN-major, i.e. as [K, rowsA] ([K, rowsB])
+                           //   row-major (its transpose); the GEMM then runs on CTA pairs only
     const float* bias;     // TWELL_RELU: per B row; GATE_SWAP: per A row; DENSE: per B row or null
     int relu;              // DENSE only
     uint32_t* stage;       // TWELL_RELU staging [rowsA, NB, stage_cap]
@@ -136,7 +141,10 @@ struct GemmArgs {
     int accumulate;        //   out_f32 += result (else =)
     const uint16_t* mask;  //   if set, [rowsA, ldm] bf16: result kept only where mask is nonzero
     int ldm;
-    float add_scalar;      //   added to every result before the mask
+    float add_scalar;      //   added to every result before the mask (fp32 and bf16 outputs)
+    float* colsum;         // DENSE, bf16 output only: if set, column sums of the (masked) fp32 results per
+                           //   128-row block: colsum[(row / 128) * ldc + col]
+    int ldc;
     int32_t* status;
 };
 // ---- Down-projection on the tensor cores over token-group unions (twell_union.cu)

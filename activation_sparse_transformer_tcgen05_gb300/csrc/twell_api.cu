@@ -109,16 +109,18 @@ size_t carve_fwd(void* ws, bool gated, int M, int F, int64_t cap, FwdWs* out, bo
 
 struct BwdWs {
     float* dpre;
+    float* part;  // per-column-slice SDDMM sums
     CscWork csc;
 };
 
-size_t carve_bwd(void* ws, int M, int F, int64_t cap, BwdWs* out)
+size_t carve_bwd(void* ws, int M, int d, int F, int64_t cap, BwdWs* out)
 {
     Carver c{static_cast<char*>(ws)};
     BwdWs w{};
     csc_plan(M, F, &w.csc.row_blocks, &w.csc.rows_per_block);
     const size_t capn = (size_t)(cap > 0 ? cap : 1);
     w.dpre = c.take<float>(capn);
+    w.part = c.take<float>(capn * (size_t)sddmm_slices(d > 0 ? d : 1));
     w.csc.masks = c.take<unsigned long long>((size_t)w.csc.row_blocks * F);
     w.csc.start = c.take<int32_t>((size_t)w.csc.row_blocks * F);
     w.csc.colcnt = c.take<int32_t>((size_t)F);
@@ -206,13 +208,13 @@ int64_t twell_buf_slots_bound(int M, int F, int T)
 
 size_t twell_workspace_bytes(int op, int M, int d, int F, int T, int64_t cap_slots)
 {
-    (void)d;
     (void)T;
     if (M <= 0 || F <= 0) return 0;
+    if (op == TWELL_OP_FFN_BWD && d <= 0) return 0;
     switch (op) {
         case TWELL_OP_FFN_FWD: return carve_fwd(nullptr, false, M, F, cap_slots, nullptr);
         case TWELL_OP_GATED_FWD: return carve_fwd(nullptr, true, M, F, cap_slots, nullptr);
-        case TWELL_OP_FFN_BWD: return carve_bwd(nullptr, M, F, cap_slots, nullptr);
+        case TWELL_OP_FFN_BWD: return carve_bwd(nullptr, M, d, F, cap_slots, nullptr);
         case TWELL_OP_HYBRID_FWD: return carve_fwd(nullptr, false, M, F, cap_slots, nullptr, true);
         default: return 0;
     }
@@ -544,14 +546,14 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
     twell_status st = check_buf(h, M, F, h->T);
     if (st != TWELL_OK) return st;
     if (h->cap_slots >= (int64_t)INT32_MAX || d > 4096) return TWELL_ERR_UNSUPPORTED;
-    const size_t need = carve_bwd(nullptr, M, F, h->cap_slots, nullptr);
+    const size_t need = carve_bwd(nullptr, M, d, F, h->cap_slots, nullptr);
     if (!ws || ws_bytes < need) return TWELL_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const TwellView tw = view_of(h);
     BwdWs w;
-    carve_bwd(ws, M, F, h->cap_slots, &w);
+    carve_bwd(ws, M, d, F, h->cap_slots, &w);
     // The column lists' first kernels read only the TwELL indices: they run on
     // a side stream under the SDDMM (fork and join by events, which stream
     // capture also records); without a side stream they run first on s.
@@ -570,7 +572,7 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
         timer_end(TWELL_SITE_CSC, s);
     }
     timer_begin(TWELL_SITE_SDDMM, s);
-    if (e == cudaSuccess) e = launch_sddmm(tw, dy, W_down, d, l1_coef, w.dpre, status, s);
+    if (e == cudaSuccess) e = launch_sddmm(tw, dy, W_down, d, l1_coef, w.dpre, w.part, status, s);
     timer_end(TWELL_SITE_SDDMM, s);
     timer_begin(TWELL_SITE_DX, s);
     if (e == cudaSuccess) e = launch_spmm_rows(tw, w.dpre, W_up, d, dx, status, s);
@@ -580,38 +582,6 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
     timer_begin(TWELL_SITE_WGRAD, s);
     if (e == cudaSuccess) e = launch_wgrad(tw, w.csc, w.dpre, x, dy, d, dW_up, dW_down, db, status, s);
     timer_end(TWELL_SITE_WGRAD, s);
-    return cuda_status(e);
-}
-
-twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const float* b, const uint16_t* W_downT,
-                                 int M, int d, int F, uint16_t* h_dense, uint16_t* y, int32_t* status, void* stream)
-{
-    if (!x || !W_up || !W_downT || !h_dense || !y || !status || !dims_ok(M, d, F)) return TWELL_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(W_up) || !aligned16(W_downT) || !aligned16(h_dense) || !aligned16(y))
-        return TWELL_ERR_INVALID_ARG;
-    const int sms = sm_count_current();
-    if (sms <= 0) return TWELL_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    GemmArgs g1{};
-    g1.rowsA = M;
-    g1.rowsB = F;
-    g1.K = d;
-    g1.bias = b;
-    g1.relu = 1;
-    g1.out = h_dense;
-    g1.ldo = F;
-    g1.status = status;
-    cudaError_t e = launch_gemm(GEMM_DENSE, x, W_up, g1, sms, s);
-    GemmArgs g2{};
-    g2.rowsA = M;
-    g2.rowsB = d;
-    g2.K = F;
-    g2.bias = nullptr;
-    g2.relu = 0;
-    g2.out = y;
-    g2.ldo = d;
-    g2.status = status;
-    if (e == cudaSuccess) e = launch_gemm(GEMM_DENSE, h_dense, W_downT, g2, sms, s);
     return cuda_status(e);
 }
 

@@ -52,7 +52,9 @@ struct Layout {
     static constexpr int BIAS_BYTES = 4 * (BN > BM ? BN : BM);
     static constexpr int MASK_OFF = BIAS_OFF + BIAS_BYTES;
     static constexpr int MASK_BYTES = 64 * 4 * 4;
-    static constexpr int TOTAL = MASK_OFF + MASK_BYTES + 1024;  // + alignment slack
+    static constexpr int COL_OFF = MASK_OFF + MASK_BYTES;
+    static constexpr int COL_BYTES = 4 * BN * 4;  // dense epilogue: per-warp column sums
+    static constexpr int TOTAL = COL_OFF + COL_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                         : (2 * BN <= 256) ? 256 : 512;
     static_assert(SUB_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
@@ -114,18 +116,25 @@ __device__ __forceinline__ void epi_twell_row(uint32_t tbase, int row, int rowsA
     }
 }
 
-// Dense epilogue of one accumulator row: bias, optional ReLU, bf16 stores.
+// Dense epilogue of one accumulator row (one thread; the 128 epilogue threads
+// hold the 128 rows of the CTA's tile): bias, optional ReLU, + add_scalar,
+// the mask, then bf16 or fp32 stores. With a.colsum (bf16 output) the warp's
+// 32 rows are summed per column by a butterfly, the four warps' sums are
+// added in warp order through s_col, and row block rt's column sums are
+// written for the tile's columns.
 template <int BN>
 __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int rowsA, int nb, const GemmArgs& a,
-                                              const float* bias_sm)
+                                              const float* bias_sm, float* s_col, int rt, int q, int et)
 {
+    const int lane = et & 31;
     const bool row_ok = row < rowsA;
     const int orow = (row_ok && a.row_map) ? a.row_map[row] : row;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t v[32];
         tmem_ld32_wait(tbase + ch * 32, v);
-        if (row_ok && a.out_f32) {
+        if (a.out_f32) {
+            if (!row_ok) continue;
             // fp32 output: + add_scalar, kept where mask is nonzero (if given),
             // added to what out_f32 holds (if accumulate)
 #pragma unroll
@@ -153,17 +162,27 @@ __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int rowsA
                     o[1] = make_float4(f[4], f[5], f[6], f[7]);
                 }
             }
-        } else if (row_ok) {
+        } else {
+            float cs[32];
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const int col = nb * BN + ch * 32 + g8 * 8;
-                if (col < a.rowsB) {
-                    float f[8];
+                const bool ok = row_ok && col < a.rowsB;
+                float f[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        f[e] = __uint_as_float(v[g8 * 8 + e]) + bias_sm[ch * 32 + g8 * 8 + e];
-                        if (a.relu) f[e] = fmaxf(f[e], 0.f);
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    f[e] = __uint_as_float(v[g8 * 8 + e]) + bias_sm[ch * 32 + g8 * 8 + e];
+                    if (a.relu) f[e] = fmaxf(f[e], 0.f);
+                    f[e] += a.add_scalar;
+                }
+                if (a.mask && ok) {
+                    const uint4 m = *reinterpret_cast<const uint4*>(a.mask + (size_t)row * a.ldm + col);
+                    const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (((mw[e >> 1] >> ((e & 1) * 16)) & 0x7fffu) == 0u) f[e] = 0.f;
+                }
+                if (ok) {
                     uint4 o;
                     o.x = pack_bf16x2(f[0], f[1]);
                     o.y = pack_bf16x2(f[2], f[3]);
@@ -171,7 +190,24 @@ __device__ __forceinline__ void epi_dense_row(uint32_t tbase, int row, int rowsA
                     o.w = pack_bf16x2(f[6], f[7]);
                     *reinterpret_cast<uint4*>(a.out + (size_t)orow * a.ldo + col) = o;
                 }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) cs[g8 * 8 + e] = ok ? f[e] : 0.f;
             }
+            if (a.colsum) {
+                transpose_reduce32(cs, lane);  // lane u: column ch * 32 + u over the warp's 32 rows
+                s_col[q * BN + ch * 32 + lane] = cs[0];
+            }
+        }
+    }
+    if (a.colsum && !a.out_f32) {
+        named_bar_sync(2, kEpiThreads);
+        // a CTA-pair tile's second half can lie wholly past the last row:
+        // row block rt exists only if it holds a row
+        const bool block_ok = rt * 128 < rowsA;
+        for (int c = et; c < BN; c += kEpiThreads) {
+            const int col = nb * BN + c;
+            if (block_ok && col < a.rowsB)
+                a.colsum[(size_t)rt * a.ldc + col] = ((s_col[c] + s_col[BN + c]) + s_col[2 * BN + c]) + s_col[3 * BN + c];
         }
     }
 }
@@ -195,6 +231,7 @@ __global__ void __launch_bounds__(192, 1)
     volatile int* epi_fail = reinterpret_cast<volatile int*>(tmem_slot + 3);
     float* bias_sm = reinterpret_cast<float*>(smem + L::BIAS_OFF);
     uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + L::MASK_OFF);
+    float* s_col = reinterpret_cast<float*>(smem + L::COL_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -414,7 +451,7 @@ __global__ void __launch_bounds__(192, 1)
                     if (total && a.nnz) atomicAdd(&a.nnz[tok0 + t], total);
                 }
             } else {  // GEMM_DENSE
-                epi_dense_row<BN>(tbase, mb * BM + 32 * q + lane, rowsA, nb, a, bias_sm);
+                epi_dense_row<BN>(tbase, mb * BM + 32 * q + lane, rowsA, nb, a, bias_sm, s_col, mb, q, et);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -468,18 +505,36 @@ struct PairLayout {
     static constexpr int NBARS = 2 * STAGES + 5;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BIAS_OFF = (MISC_OFF + 16 + 15) & ~15;
-    static constexpr int TOTAL = BIAS_OFF + PAIR_N * 4 + 1024;  // + alignment slack
+    static constexpr int COL_OFF = BIAS_OFF + PAIR_N * 4;
+    static constexpr int TOTAL = COL_OFF + 4 * PAIR_N * 4 + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * PAIR_N;
     static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
 };
 
-template <int MODE, int STAGES, int CAP = PAIR_N>
+// Operands stored MN-major (A_MN, B_MN: the matrix is given as its transpose,
+// [K, rows] row-major) arrive as two 64-row x 64-element TMA boxes per CTA
+// half and k-block, 8 KB apart: the 128-byte-swizzled MN-major layout whose
+// 64-element blocks along MN are 8 KB apart and whose 8-row groups along K
+// are 1024 bytes apart. A 16-deep K step then advances 2048 bytes instead of
+// the K-major operand's 32.
+constexpr int kMnBox = 64;
+
+__device__ __forceinline__ uint64_t operand_desc(bool mn, uint32_t addr)
+{
+    return mn ? sw128_mnmajor_desc(addr, kMnBox * BK * 2) : sw128_kmajor_desc(addr);
+}
+
+template <int MODE, int STAGES, int CAP = PAIR_N, bool A_MN = false, bool B_MN = false>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a)
 {
     static_assert(MODE == GEMM_TWELL_RELU || MODE == GEMM_DENSE, "row-wise epilogues only");
+    static_assert(MODE == GEMM_DENSE || (!A_MN && !B_MN), "MN-major operands: dense epilogue only");
     using L = PairLayout<STAGES>;
-    constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, PAIR_N);
+    constexpr uint32_t IDESC =
+        idesc_bf16_f32(PAIR_M, PAIR_N) | (A_MN ? kIdescAMn : 0u) | (B_MN ? kIdescBMn : 0u);
+    constexpr uint64_t A_KSTEP = A_MN ? (16u * 128u) >> 4 : 2u;  // descriptor units (16 B) per 16-deep K step
+    constexpr uint64_t B_KSTEP = B_MN ? (16u * 128u) >> 4 : 2u;
     constexpr int kEpiWarps = 2 * (kEpiThreads / 32);  // tmem-empty arrivals: both CTAs
     extern __shared__ uint8_t smem_raw[];
     // Same offset in both CTAs (same kernel, same static shared memory), as the
@@ -495,6 +550,7 @@ __global__ void __launch_bounds__(192, 1)
     volatile int* skip = reinterpret_cast<volatile int*>(tmem_slot + 2);
     volatile int* epi_fail = reinterpret_cast<volatile int*>(tmem_slot + 3);
     float* bias_sm = reinterpret_cast<float*>(smem + L::BIAS_OFF);
+    float* s_col = reinterpret_cast<float*>(smem + L::COL_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -556,8 +612,19 @@ __global__ void __launch_bounds__(192, 1)
                     uint8_t* sa = smem + stage * L::STAGE_BYTES;
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
                     const uint32_t fb = full_leader + 8u * (uint32_t)stage;
-                    tma_load_2d_pair(sa, &tmA, kb * BK, mb * PAIR_M + (int)rank * HALF, fb);
-                    tma_load_2d_pair(sa + L::A_BYTES, &tmB, kb * BK, nb * PAIR_N + (int)rank * HALF, fb);
+                    const int ma = mb * PAIR_M + (int)rank * HALF, nbr = nb * PAIR_N + (int)rank * HALF;
+                    if (A_MN) {
+                        tma_load_2d_pair(sa, &tmA, ma, kb * BK, fb);
+                        tma_load_2d_pair(sa + kMnBox * BK * 2, &tmA, ma + kMnBox, kb * BK, fb);
+                    } else {
+                        tma_load_2d_pair(sa, &tmA, kb * BK, ma, fb);
+                    }
+                    if (B_MN) {
+                        tma_load_2d_pair(sa + L::A_BYTES, &tmB, nbr, kb * BK, fb);
+                        tma_load_2d_pair(sa + L::A_BYTES + kMnBox * BK * 2, &tmB, nbr + kMnBox, kb * BK, fb);
+                    } else {
+                        tma_load_2d_pair(sa + L::A_BYTES, &tmB, kb * BK, nbr, fb);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -596,11 +663,11 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * L::STAGE_BYTES);
-                    const uint64_t adesc = sw128_kmajor_desc(sa);
-                    const uint64_t bdesc = sw128_kmajor_desc(sa + L::A_BYTES);
+                    const uint64_t adesc = operand_desc(A_MN, sa);
+                    const uint64_t bdesc = operand_desc(B_MN, sa + L::A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        umma_bf16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb | k) != 0);
+                        umma_bf16_pair(d_tmem, adesc + A_KSTEP * k, bdesc + B_KSTEP * k, IDESC, (kb | k) != 0);
                     umma_commit_pair(&empty[stage], 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -644,7 +711,7 @@ __global__ void __launch_bounds__(192, 1)
             if constexpr (MODE == GEMM_TWELL_RELU)
                 epi_twell_row<PAIR_N, CAP>(tbase, row, rowsA, nb, a, bias_sm);
             else
-                epi_dense_row<PAIR_N>(tbase, row, rowsA, nb, a, bias_sm);
+                epi_dense_row<PAIR_N>(tbase, row, rowsA, nb, a, bias_sm, s_col, 2 * mb + (int)rank, q, et);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
@@ -716,7 +783,21 @@ cudaError_t run(const uint16_t* A, const uint16_t* B, const GemmArgs& a, int tok
 }
 
 // Clusters of two that can be resident at once for this kernel (0 = none).
-template <int MODE, int STAGES, int CAP>
+// [K, mn] bf16 row-major (an MN-major operand), box = 64 (MN) x 64 (K), 128-byte swizzle, zero fill.
+bool make_map_mn(CUtensorMap* m, const void* ptr, int mn, int K)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)mn, (cuuint64_t)K};
+    cuuint64_t strides[1] = {(cuuint64_t)mn * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kMnBox, (cuuint32_t)BK};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, int STAGES, int CAP, bool A_MN, bool B_MN>
 int pair_capacity(cudaLaunchConfig_t cfg)
 {
     static int cached[64] = {0};
@@ -725,7 +806,7 @@ int pair_capacity(cudaLaunchConfig_t cfg)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (!known[dev]) {
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<MODE, STAGES, CAP>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<MODE, STAGES, CAP, A_MN, B_MN>, &cfg) != cudaSuccess) {
             (void)cudaGetLastError();
             n = 0;
         }
@@ -737,12 +818,12 @@ int pair_capacity(cudaLaunchConfig_t cfg)
 
 // Launches the pair kernel; *launched = false (and nothing enqueued) when no
 // cluster of two fits, so the caller can take the single-CTA kernel.
-template <int MODE, int STAGES, int CAP = PAIR_N>
+template <int MODE, int STAGES, int CAP = PAIR_N, bool A_MN = false, bool B_MN = false>
 cudaError_t run_pair(const uint16_t* A, const uint16_t* B, const GemmArgs& a, cudaStream_t s, bool* launched)
 {
     using L = PairLayout<STAGES>;
     *launched = false;
-    auto kern = k_gemm_pair<MODE, STAGES, CAP>;
+    auto kern = k_gemm_pair<MODE, STAGES, CAP, A_MN, B_MN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -757,10 +838,12 @@ cudaError_t run_pair(const uint16_t* A, const uint16_t* B, const GemmArgs& a, cu
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int cap = pair_capacity<MODE, STAGES, CAP>(cfg);
+    const int cap = pair_capacity<MODE, STAGES, CAP, A_MN, B_MN>(cfg);
     if (cap <= 0) return cudaSuccess;
     CUtensorMap ma, mb;
-    if (!make_map(&ma, A, a.rowsA, a.K, HALF) || !make_map(&mb, B, a.rowsB, a.K, HALF)) return cudaErrorInvalidValue;
+    const bool ok_a = A_MN ? make_map_mn(&ma, A, a.rowsA, a.K) : make_map(&ma, A, a.rowsA, a.K, HALF);
+    const bool ok_b = B_MN ? make_map_mn(&mb, B, a.rowsB, a.K) : make_map(&mb, B, a.rowsB, a.K, HALF);
+    if (!ok_a || !ok_b) return cudaErrorInvalidValue;
     const int tiles = ((a.rowsA + PAIR_M - 1) / PAIR_M) * ((a.rowsB + PAIR_N - 1) / PAIR_N);
     cfg.gridDim = dim3(2 * (tiles < cap ? tiles : cap), 1, 1);
     count_launches(1);
@@ -802,8 +885,20 @@ cudaError_t launch_gemm(int mode, const uint16_t* A, const uint16_t* B, const Ge
                 case 32: return launch_row_wise<GEMM_TWELL_RELU, 32>(A, B, a, sm_count, s);
                 default: return cudaErrorInvalidValue;
             }
-        case GEMM_DENSE:
-            return launch_row_wise<GEMM_DENSE, 256>(A, B, a, sm_count, s);
+        case GEMM_DENSE: {
+            if (!a.a_mn && !a.b_mn) return launch_row_wise<GEMM_DENSE, 256>(A, B, a, sm_count, s);
+            // MN-major operands: CTA pairs only
+            bool launched = false;
+            cudaError_t e;
+            if (a.a_mn && a.b_mn)
+                e = run_pair<GEMM_DENSE, 6, PAIR_N, true, true>(A, B, a, s, &launched);
+            else if (a.b_mn)
+                e = run_pair<GEMM_DENSE, 6, PAIR_N, false, true>(A, B, a, s, &launched);
+            else
+                e = run_pair<GEMM_DENSE, 6, PAIR_N, true, false>(A, B, a, s, &launched);
+            if (e != cudaSuccess) return e;
+            return launched ? cudaSuccess : cudaErrorNotSupported;
+        }
         case GEMM_GATE_SWAP: {
             // B = x: token chunks of at most 64 rows, each a separate launch.
             const int bn = gemm_block_n(mode, a.rowsB);

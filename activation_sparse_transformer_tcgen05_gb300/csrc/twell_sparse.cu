@@ -116,23 +116,6 @@ __device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b)
     return s0 + s1;
 }
 
-// After this, lane u holds the sum over all 32 lanes of v[u] (in v[0]): a
-// butterfly where each step keeps the half of the values that belongs to the
-// lane's side and adds the partner's copy of that half (31 shuffles in all).
-__device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane)
-{
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < off; ++i) {
-            const float send = upper ? v[i] : v[i + off];
-            const float keep = upper ? v[i + off] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-    }
-}
-
 // sum_k a[k] * b[k] over 8 bf16 pairs
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& b)
 {
@@ -898,63 +881,187 @@ __global__ void __launch_bounds__((SPLIT > kWarps ? SPLIT : kWarps) * 32) k_spmm
     }
 }
 
-// Backward SDDMM: dpre[slot] = dy[r] . W[idx] + l1 on the stored slots of
-// row r, 0 on its padding slots. A block per row, a warp per 256-column slice
-// of d (G = ceil(d/256) warps). The row's entries go in batches of 32 (lane u
-// holding entry u's column); each warp forms its slice's share of the batch's
-// 32 dot products (16 rows of W in flight at a time, two fp32 chains per
-// product on bf16 factors) and transpose_reduce32 leaves entry u's slice sum in
-// lane u. Warp 0 adds the G slice sums in slice order through shared memory.
-constexpr int kSddmmMaxSlices = 16;  // d <= 4096
-
-__global__ void __launch_bounds__(kSddmmMaxSlices * 32) k_sddmm_rows(TwellView tw, const uint16_t* __restrict__ dy,
-                                                                     const uint16_t* __restrict__ W, int d, float l1,
-                                                                     float* __restrict__ dpre, const int32_t* status)
+// The same product for many rows (M >= 256), column-group-major: warp task
+// (column group g of CH x 256 columns, row r) with task = g * M + r, so that at
+// any time the grid works through one group's slice of W (F x CH x 256 bf16,
+// 8 or 16 MB at d_ff = 16384) and that slice stays in L2, whatever the size of
+// W. Lane l holds columns g * 256 CH + 256 c + 8 l .. +7 of chunk c; entries
+// come 4 at a time (4 CH 128-bit loads in flight per lane).
+template <int CH>
+__global__ void __launch_bounds__(kWarps * 32) k_spmm_cols(TwellView tw, const float* __restrict__ vals_f32,
+                                                           const uint16_t* __restrict__ W, int d,
+                                                           uint16_t* __restrict__ y, const int32_t* status)
 {
-    __shared__ float s_part[kSddmmMaxSlices][32];
-    const int r = blockIdx.x;
-    const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = blockDim.x >> 5;
+    constexpr int GW = 256 * CH;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t task = (int64_t)blockIdx.x * kWarps + warp;
     if (has_error(status) || over_capacity(tw)) return;  // uniform across the block
+    const int g = (int)(task / tw.M), r = (int)(task % tw.M);
+    if (g * GW >= d) return;
+    int c0[CH];
+    bool ok[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        c0[c] = g * GW + c * 256 + lane * 8;
+        ok[c] = c0[c] < d;
+    }
+    float acc[CH][8];
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[c][e] = 0.f;
     int Kt;
     const int64_t base = row_base(tw, r, &Kt);
     const int n = tw.nnz[r];
-    const int col = g * 256 + lane * 8;
-    const bool col_ok = col < d;
-    const uint4 a = col_ok ? ldg16(dy + (size_t)r * d + col) : make_uint4(0, 0, 0, 0);
-    const uint16_t* Wc = W + (col_ok ? col : 0);
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        const int m = min(32, n - k0);
+        int jl = 0;
+        float vl = 0.f;
+        uint32_t vb = 0;
+        if (lane < m) {
+            jl = tw.idx[base + k0 + lane];
+            if (vals_f32)
+                vl = vals_f32[base + k0 + lane];
+            else
+                vb = tw.val[base + k0 + lane];
+        }
+        int u = 0;
+        for (; u + 4 <= m; u += 4) {
+            uint4 w[4][CH];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int jj = __shfl_sync(0xffffffffu, jl, u + q);
+#pragma unroll
+                for (int c = 0; c < CH; ++c)
+                    w[q][c] = ok[c] ? ldg16(W + (size_t)jj * d + c0[c]) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (vals_f32) {
+                    const float v = __shfl_sync(0xffffffffu, vl, u + q);
+#pragma unroll
+                    for (int c = 0; c < CH; ++c) fma8(acc[c], v, w[q][c]);
+                } else {
+                    const uint32_t v = __shfl_sync(0xffffffffu, vb, u + q);
+#pragma unroll
+                    for (int c = 0; c < CH; ++c) fma8_bf16(acc[c], v, w[q][c]);
+                }
+            }
+        }
+        for (; u < m; ++u) {
+            const int jj = __shfl_sync(0xffffffffu, jl, u);
+            uint4 w[CH];
+#pragma unroll
+            for (int c = 0; c < CH; ++c) w[c] = ok[c] ? ldg16(W + (size_t)jj * d + c0[c]) : make_uint4(0, 0, 0, 0);
+            if (vals_f32) {
+                const float v = __shfl_sync(0xffffffffu, vl, u);
+#pragma unroll
+                for (int c = 0; c < CH; ++c) fma8(acc[c], v, w[c]);
+            } else {
+                const uint32_t v = __shfl_sync(0xffffffffu, vb, u);
+#pragma unroll
+                for (int c = 0; c < CH; ++c) fma8_bf16(acc[c], v, w[c]);
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        if (ok[c]) {
+            uint4 o;
+            o.x = pack_bf16x2(acc[c][0], acc[c][1]);
+            o.y = pack_bf16x2(acc[c][2], acc[c][3]);
+            o.z = pack_bf16x2(acc[c][4], acc[c][5]);
+            o.w = pack_bf16x2(acc[c][6], acc[c][7]);
+            *reinterpret_cast<uint4*>(y + (size_t)r * d + c0[c]) = o;
+        }
+    }
+}
+
+// Backward SDDMM over column slices of NCH x 256 columns: warp task (slice s,
+// row r), task = s * M + r (slice-major, so one slice of W_down stays in L2).
+// The lane holds its 8 NCH columns of dy[r] in registers; the row's entries
+// go in batches of 32, two at a time (2 NCH 128-bit loads in flight per
+// lane), each lane forming its columns' share of both dot products;
+// transpose_reduce32 then leaves entry u's slice sum in lane u, written to
+// part[s * cap + slot]. k_sddmm_combine adds the slices in order.
+template <int NCH>
+__global__ void __launch_bounds__(kWarps * 32) k_sddmm_slices(TwellView tw, const uint16_t* __restrict__ dy,
+                                                              const uint16_t* __restrict__ W, int d, int nslices,
+                                                              float* __restrict__ part, const int32_t* status)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t task = (int64_t)blockIdx.x * kWarps + warp;
+    if (has_error(status) || over_capacity(tw)) return;  // uniform across the block
+    const int sl = (int)(task / tw.M), r = (int)(task % tw.M);
+    if (sl >= nslices) return;
+    int col[NCH];
+    bool ok[NCH];
+    uint4 a[NCH];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        col[c] = (sl * NCH + c) * 256 + lane * 8;
+        ok[c] = col[c] < d;
+        a[c] = ok[c] ? ldg16(dy + (size_t)r * d + col[c]) : make_uint4(0, 0, 0, 0);
+    }
+    int Kt;
+    const int64_t base = row_base(tw, r, &Kt);
+    const int n = tw.nnz[r];
+    float* out = part + (size_t)sl * (size_t)tw.cap + base;
     for (int k0 = 0; k0 < n; k0 += 32) {
         const int m = min(32, n - k0);
         const int jl = tw.idx[base + k0 + (lane < m ? lane : 0)];
         float v[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (h * 16 < m) {
-                uint4 w[16];
+        for (int u = 0; u < 32; u += 2) {
+            if (u < m) {  // warp-uniform
+                const int j0 = __shfl_sync(0xffffffffu, jl, u);
+                const int j1 = __shfl_sync(0xffffffffu, jl, u + 1 < m ? u + 1 : u);
+                uint4 w0[NCH], w1[NCH];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int jj = __shfl_sync(0xffffffffu, jl, h * 16 + q);
-                    w[q] = col_ok ? ldg16(Wc + (size_t)jj * d) : make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < NCH; ++c) {
+                    w0[c] = ok[c] ? ldg16(W + (size_t)j0 * d + col[c]) : make_uint4(0, 0, 0, 0);
+                    w1[c] = ok[c] ? ldg16(W + (size_t)j1 * d + col[c]) : make_uint4(0, 0, 0, 0);
                 }
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int q = 0; q < 16; ++q) v[h * 16 + q] = dot8_bf16(a, w[q]);
+                for (int c = 0; c < NCH; ++c) {
+                    s0 += dot8_bf16(a[c], w0[c]);
+                    s1 += dot8_bf16(a[c], w1[c]);
+                }
+                v[u] = s0;
+                v[u + 1] = u + 1 < m ? s1 : 0.f;
             } else {
-#pragma unroll
-                for (int q = 0; q < 16; ++q) v[h * 16 + q] = 0.f;
+                v[u] = 0.f;
+                v[u + 1] = 0.f;
             }
         }
         transpose_reduce32(v, lane);
-        s_part[g][lane] = v[0];
-        __syncthreads();
-        if (g == 0) {
-            float tot = 0.f;
-            for (int q = 0; q < G; ++q) tot += s_part[q][lane];
-            if (lane < m) dpre[base + k0 + lane] = tot + l1;
-        }
-        __syncthreads();
+        if (lane < m) out[k0 + lane] = v[0];
     }
-    if (g == 0)
-        for (int k = n + lane; k < Kt; k += 32) dpre[base + k] = 0.f;
+}
+
+// dpre[slot] = (part[0][slot] + part[1][slot] + ...) + l1 on the stored slots
+// of row r (slices added in order), 0 on its padding. One warp per row.
+__global__ void __launch_bounds__(kWarps * 32) k_sddmm_combine(TwellView tw, const float* __restrict__ part,
+                                                               int nslices, float l1, float* __restrict__ dpre,
+                                                               const int32_t* status)
+{
+    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
+    int Kt;
+    const int64_t base = row_base(tw, r, &Kt);
+    const int n = tw.nnz[r];
+    for (int k = lane; k < Kt; k += 32) {
+        const int64_t slot = base + k;
+        float v = 0.f;
+        if (k < n) {
+            v = part[slot];
+            for (int sl = 1; sl < nslices; ++sl) v += part[(size_t)sl * (size_t)tw.cap + slot];
+            v += l1;
+        }
+        dpre[slot] = v;
+    }
 }
 
 // Row dot products on the stored entries: for entry (r, k) with column j,
@@ -1296,11 +1403,18 @@ cudaError_t launch_fill_staged_gate(const uint2* stage, const int32_t* stage_cnt
 cudaError_t launch_spmm_rows(const TwellView& tw, const float* vals_f32, const uint16_t* W, int d, uint16_t* y,
                              int32_t* status, cudaStream_t s)
 {
-    const int64_t tasks = (int64_t)tw.M * ((d + 255) / 256);
     count_launches(1);
     if (tw.M >= 256) {
-        k_spmm_rows<1><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
+        // two 256-column chunks per lane when d has them, else one
+        if (d > 256) {
+            const int64_t tasks = (int64_t)tw.M * ((d + 511) / 512);
+            k_spmm_cols<2><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
+        } else {
+            const int64_t tasks = (int64_t)tw.M * ((d + 255) / 256);
+            k_spmm_cols<1><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
+        }
     } else {
+        const int64_t tasks = (int64_t)tw.M * ((d + 255) / 256);
         k_spmm_rows<16><<<(unsigned)tasks, 16 * 32, 0, s>>>(tw, vals_f32, W, d, y, status);
     }
     return cudaGetLastError();
@@ -1342,13 +1456,25 @@ static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const
     return cudaGetLastError();
 }
 
+int sddmm_slices(int d) { return (d + 1023) / 1024; }
+
 cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float l1, float* dpre,
-                         int32_t* status, cudaStream_t s)
+                         float* part, int32_t* status, cudaStream_t s)
 {
-    const int G = (d + 255) / 256;
-    if (G > kSddmmMaxSlices) return cudaErrorInvalidValue;
-    count_launches(1);
-    k_sddmm_rows<<<tw.M, G * 32, 0, s>>>(tw, dy, W, d, l1, dpre, status);
+    // slices of up to four 256-column chunks (1024 columns)
+    const int nch_total = (d + 255) / 256;
+    const int nch = nch_total < 4 ? nch_total : 4;
+    const int nsl = (nch_total + nch - 1) / nch;
+    if (nsl > sddmm_slices(d)) return cudaErrorInvalidValue;
+    const int64_t tasks = (int64_t)tw.M * nsl;
+    count_launches(2);
+    switch (nch) {
+        case 1: k_sddmm_slices<1><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, dy, W, d, nsl, part, status); break;
+        case 2: k_sddmm_slices<2><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, dy, W, d, nsl, part, status); break;
+        case 3: k_sddmm_slices<3><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, dy, W, d, nsl, part, status); break;
+        default: k_sddmm_slices<4><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, dy, W, d, nsl, part, status); break;
+    }
+    k_sddmm_combine<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, part, nsl, l1, dpre, status);
     return cudaGetLastError();
 }
 

@@ -12,7 +12,10 @@
 // stand-in, not a device address (a kernel handed it would fault, or on
 // systems where the GPU can read host memory silently use the wrong memory).
 // The device address is therefore looked up with cudaGetSymbolAddress, once
-// per device, with that device current, on the first call made on it.
+// per device, with that device current, on the first call made on it. The
+// cached address belongs to the device's current context: after a
+// cudaDeviceReset the module may load at another address, so a process that
+// resets a device must not call this entry point on it again.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,11 +35,17 @@ void* g_ws_ptr[kMaxDevices] = {nullptr};
 twell_status static_ws_address(void** out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TWELL_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();  // leave no pending error for the next, unrelated call
+        return TWELL_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_ws_ptr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return TWELL_ERR_CUDA;
+        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            return TWELL_ERR_CUDA;
+        }
         g_ws_ptr[dev] = p;
     }
     *out = g_ws_ptr[dev];
@@ -50,8 +59,12 @@ extern "C" twell_status twell_ffn_fwd_static_ws(const uint16_t* x, const uint16_
                                                 const twell_buf* h_out, uint16_t* y, int32_t* status, void* stream)
 {
     if (!h_out || M <= 0 || d <= 0 || F <= 0 || T <= 0) return TWELL_ERR_INVALID_ARG;
-    const int op = W_gate ? TWELL_OP_GATED_FWD : TWELL_OP_FFN_FWD;
-    const size_t need = twell_workspace_bytes(op, M, d, F, T, h_out->cap_slots);
+    // The smallest workspace the forward accepts: the gated layout, or the ReLU
+    // layout at its smallest staging capacity (32 entries per row and 256-column
+    // block). twell_ffn_fwd then takes the largest staging the array holds.
+    const size_t need = W_gate ? twell_workspace_bytes(TWELL_OP_GATED_FWD, M, d, F, T, h_out->cap_slots)
+                               : twell_fwd_workspace_bytes(M, d, F, T, h_out->cap_slots, 32);
+    if (need == 0) return TWELL_ERR_INVALID_ARG;
     if (need > (size_t)TWELL_STATIC_WS_BYTES) return TWELL_ERR_WORKSPACE;  // problem too large for the array
     void* ws = nullptr;
     const twell_status st = static_ws_address(&ws);

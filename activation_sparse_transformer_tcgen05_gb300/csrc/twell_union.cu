@@ -253,22 +253,6 @@ struct ULayout {
     static_assert(EA >= 1 && EA < NE, "a bucket slot is refilled only after its A tile was built");
 };
 
-// Shared-memory descriptor of an MN-major operand written with the 128-byte
-// swizzle: 64 contiguous elements (128 B) along MN per row, 8 rows along K
-// per 1024-byte atom; `mn_stride` bytes between 64-element blocks along MN
-// (leading byte offset), 1024 bytes between 8-row groups along K (stride
-// byte offset).
-__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t mn_stride)
-{
-    uint64_t d = 0;
-    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
-    d |= (uint64_t)1u << 46;
-    d |= (uint64_t)2u << 61;
-    return d;
-}
-
 // Arrive once on `bar` when every cp.async this thread issued so far has
 // completed; the arrival counts toward the barrier's expected count.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
@@ -285,7 +269,7 @@ __global__ void __launch_bounds__(kUnionGemmThreads, 1)
 {
     using L = ULayout<BN, NBS, NE, EA, NA>;
     // bf16 A (K-major) and B (MN-major: bit 16), fp32 D, M = 128, N = BN
-    constexpr uint32_t IDESC = idesc_bf16_f32(UG, BN) | (1u << 16);
+    constexpr uint32_t IDESC = idesc_bf16_f32(UG, BN) | kIdescBMn;
     constexpr int CPU = BN / 8;           // 16-byte pieces per gathered row
     constexpr int UPW = 32 / CPU;         // rows per warp instruction
     constexpr int NCP = UBK * CPU / kLoaders;  // pieces per loader thread per k-block

@@ -44,7 +44,7 @@ def train(steps: int = 1000, M: int = 4096, d: int = 1024, F: int = 4096, T: int
     Ft = teacher_units
     Tu = torch.randn(Ft, d, device=dev, generator=g) / d ** 0.5
     Td = torch.randn(Ft, d, device=dev, generator=g) / Ft ** 0.5
-    teacher = (_bits(Tu), torch.zeros(Ft, device=dev), _bits(Td.t().contiguous()))
+    teacher = (_bits(Tu), torch.zeros(Ft, device=dev), _bits(Td))
     params = [torch.randn(F, d, device=dev, generator=g) / d ** 0.5,  # W_up
               torch.zeros(F, device=dev),                              # b
               torch.randn(F, d, device=dev, generator=g) / F ** 0.5]  # W_down

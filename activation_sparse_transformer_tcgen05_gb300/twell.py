@@ -23,8 +23,8 @@ OP_PACK, OP_SPMM_DOWN, OP_FFN_FWD, OP_FFN_BWD, OP_GATED_FWD, OP_HYBRID_FWD = 0, 
 EXPORTED_SYMBOLS = (
     "twell_status_string", "twell_buf_slots_bound", "twell_workspace_bytes", "twell_device_sm_count",
     "twell_pack", "twell_up_pack", "twell_spmm_down", "twell_ffn_fwd", "twell_ffn_bwd",
-    "twell_dense_ffn_fwd", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
-    "twell_set_kernel_timer", "twell_gather_probe", "twell_hybrid_up_pack", "twell_hybrid_spmm_down",
+    "twell_dense_ffn_fwd", "twell_dense_ffn_bwd", "twell_dense_bwd_workspace_bytes", "twell_kernel_launches", "twell_check", "twell_ffn_fwd_static_ws",
+    "twell_set_kernel_timer", "twell_hybrid_up_pack", "twell_hybrid_spmm_down",
     "twell_hybrid_ffn_fwd", "twell_fwd_workspace_bytes", "twell_hybrid_bwd_workspace_bytes", "twell_hybrid_ffn_bwd",
     "twell_wait_selftest", "twell_spmm_down_tc_workspace_bytes", "twell_spmm_down_tc",
 )
@@ -99,6 +99,10 @@ def load_library(path: str | None = None):
     lib.twell_ffn_bwd.argtypes = [P, P, P, BUFP, P, I32, F32, P, P, P, P, P, SZ, P, P]
     lib.twell_dense_ffn_fwd.restype = I32
     lib.twell_dense_ffn_fwd.argtypes = [P, P, P, P, I32, I32, I32, P, P, P, P]
+    lib.twell_dense_bwd_workspace_bytes.restype = SZ
+    lib.twell_dense_bwd_workspace_bytes.argtypes = [I32, I32, I32]
+    lib.twell_dense_ffn_bwd.restype = I32
+    lib.twell_dense_ffn_bwd.argtypes = [P, P, P, P, P, I32, I32, I32, F32, P, P, P, P, P, SZ, P, P]
     lib.twell_ffn_fwd_static_ws.restype = I32
     lib.twell_ffn_fwd_static_ws.argtypes = [P, P, P, P, P, I32, I32, I32, I32, BUFP, P, P, P]
     lib.twell_hybrid_up_pack.restype = I32
@@ -111,8 +115,6 @@ def load_library(path: str | None = None):
     lib.twell_hybrid_bwd_workspace_bytes.argtypes = [I32, I32, I32, I32, I64, I32]
     lib.twell_hybrid_ffn_bwd.restype = I32
     lib.twell_hybrid_ffn_bwd.argtypes = [P, P, P, P, BUFP, OVP, P, I32, F32, P, P, P, P, P, SZ, P, P]
-    lib.twell_gather_probe.restype = I32
-    lib.twell_gather_probe.argtypes = [P, I32, I32, P, I32, I32, P, P]
     lib.twell_wait_selftest.restype = I32
     lib.twell_wait_selftest.argtypes = [I32, P, P, P]
     lib.twell_check.restype = I32
@@ -231,17 +233,6 @@ def twell_set_kernel_timer(site: int, ev_begin=None, ev_end=None):
     b = ctypes.c_void_p(ev_begin.cuda_event) if ev_begin is not None else None
     e = ctypes.c_void_p(ev_end.cuda_event) if ev_end is not None else None
     _check(load_library().twell_set_kernel_timer(int(site), b, e), "twell_set_kernel_timer")
-
-
-def twell_gather_probe(W: torch.Tensor, idx: torch.Tensor, sink: torch.Tensor, stream=None):
-    """The sparse kernels' row-gather access pattern alone (measurement aid):
-    W [F, d] bf16 bits, idx [rows, nnz] int32, sink [rows * ceil(d/256)] float32."""
-    F, d = W.shape
-    rows, nnz = idx.shape
-    _check(load_library().twell_gather_probe(
-        _ptr(W, "W", bytes_per_elem=2, numel=F * d), F, d, _ptr(idx, "idx", bytes_per_elem=4, numel=rows * nnz),
-        rows, nnz, _ptr(sink, "sink", bytes_per_elem=4, numel=rows * ((d + 255) // 256)), _stream(stream)),
-        "twell_gather_probe")
 
 
 def twell_wait_selftest(which: int, scratch, status, stream=None):
@@ -370,15 +361,34 @@ def twell_ffn_bwd(x, W_up, W_down, h: TwellBuffers, dy, l1: float, dx, dW_up, dW
         _stream(stream)), "twell_ffn_bwd")
 
 
-def twell_dense_ffn_fwd(x, W_up, b, W_downT, h_dense, y, status, stream=None):
+def twell_dense_ffn_fwd(x, W_up, b, W_down, h_dense, y, status, stream=None):
+    """The dense baseline layer: h_dense = bf16(relu(x W_up^T + b)), y = h_dense W_down."""
     M, d = x.shape
     F = W_up.shape[0]
     _check(load_library().twell_dense_ffn_fwd(
         _ptr(x, "x", bytes_per_elem=2), _ptr(W_up, "W_up", bytes_per_elem=2, numel=F * d),
-        _ptr(b, "b", bytes_per_elem=4, numel=F), _ptr(W_downT, "W_downT", bytes_per_elem=2, numel=F * d),
+        _ptr(b, "b", bytes_per_elem=4, numel=F), _ptr(W_down, "W_down", bytes_per_elem=2, numel=F * d),
         M, d, F, _ptr(h_dense, "h_dense", bytes_per_elem=2, numel=M * F),
         _ptr(y, "y", bytes_per_elem=2, numel=M * d), _ptr(status, "status", bytes_per_elem=4),
         _stream(stream)), "twell_dense_ffn_fwd")
+
+
+def twell_dense_bwd_workspace_bytes(M: int, d: int, F: int) -> int:
+    return int(load_library().twell_dense_bwd_workspace_bytes(M, d, F))
+
+
+def twell_dense_ffn_bwd(x, W_up, W_down, h_dense, dy, l1: float, dx, dW_up, dW_down, db, ws, status, stream=None):
+    """Backward of the dense baseline layer (same loss and gradients as twell_ffn_bwd)."""
+    M, d = x.shape
+    F = W_up.shape[0]
+    _check(load_library().twell_dense_ffn_bwd(
+        _ptr(x, "x", bytes_per_elem=2, numel=M * d), _ptr(W_up, "W_up", bytes_per_elem=2, numel=F * d),
+        _ptr(W_down, "W_down", bytes_per_elem=2, numel=F * d),
+        _ptr(h_dense, "h_dense", bytes_per_elem=2, numel=M * F), _ptr(dy, "dy", bytes_per_elem=2, numel=M * d),
+        M, d, F, float(l1), _ptr(dx, "dx", bytes_per_elem=2, numel=M * d),
+        _ptr(dW_up, "dW_up", bytes_per_elem=4, numel=F * d), _ptr(dW_down, "dW_down", bytes_per_elem=4, numel=F * d),
+        _ptr(db, "db", bytes_per_elem=4, numel=F), _ptr(ws, "ws"), ws.numel() * ws.element_size(),
+        _ptr(status, "status", bytes_per_elem=4), _stream(stream)), "twell_dense_ffn_bwd")
 
 
 def twell_check(status: torch.Tensor, stream=None) -> int:

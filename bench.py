@@ -1,9 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the TwELL activation-sparse feed-forward hot path on one GB300.
 
-One step = the whole hot path over one batch of the inference workload
-(M=4096 tokens, d_model=2048, d_ff=8192, ReLU, bias -2.33 -> ~99 % of the hidden
-activations zero, TwELL tiles of 128 rows, L1 coefficient 1e-4, dy ~ N(0,1)):
+One step = the whole hot path over one batch of the training workload
+(M=16384 tokens, d_model=4096, d_ff=16384, ReLU, bias -2.33 -> ~99 % of the
+hidden activations zero, TwELL tiles of 128 rows, dy ~ N(0,1), L1 coefficient
+1e-4 on h):
 
     twell_up_pack    tcgen05 up-projection, TwELL built in its epilogue (a1-a3)
     twell_spmm_down  y = TwELL x W_down                                     (a4)
@@ -11,8 +12,12 @@ activations zero, TwELL tiles of 128 rows, L1 coefficient 1e-4, dy ~ N(0,1)):
 
 Inputs are resident in HBM when the timed region starts; L2 is flushed (a
 512 MB write, then a 512 MB read so that what stays in L2 is clean) between
-timed steps. Every stage is timed with CUDA events on the
-stream it runs on. Prints one JSON line (rank 0).
+timed steps. Every stage is timed with CUDA events on the stream it runs on.
+Prints one JSON line (rank 0). Besides the headline it reports, on the same
+GPU: the forward alone on the inference workload (4096 x 2048 x 8192), the
+same layer computed densely with this build's tcgen05 GEMMs (forward and
+backward), the gated decode batches, the sparsity/skew sweep, energy per
+token, peak memory, and the oracle on the host cores.
 
 --impl reference times the CPU oracle (plain C, fp64) on the host cores on a
 bounded sample of the same workload instead.
@@ -20,10 +25,12 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
 import os
+import shutil
 import statistics
 import subprocess
 import sys
@@ -39,12 +46,20 @@ import synthetic as syn  # noqa: E402
 
 METRIC = "sparse-FFN tokens/s fwd & fwd+bwd at 99% sparsity; % of HBM/tensor roofline"
 UNIT = "tokens/s"
-CONFIG_NAME = "inference"
+CONFIG_NAME = "training"
 STAGE_CAP = 32
-WORKLOAD = ("inference FFN layer: M=4096 tokens, d_model=2048, d_ff=8192, bf16, ReLU, bias=-2.33 "
-            "(~99% sparse), TwELL tile=128 rows, fp32 accumulation; step = fwd + bwd (dy~N(0,1), L1=1e-4)")
+WORKLOAD = ("training step: M=16384 tokens, d_model=4096, d_ff=16384, bf16, ReLU, bias=-2.33 (~99% sparse), "
+            "dy~N(0,1); fwd + bwd (y, dx, dW_up, dW_down, db) with L1 coefficient 1e-4 on h, TwELL tile=128 rows, "
+            "fp32 accumulation")
 L1 = 1e-4
 FLUSH_BYTES = 512 << 20
+# The pages' own end-to-end numbers (H100, trained 0.5B-2B models): context, not the target.
+PAGES_CONTEXT = {
+    "inference_throughput_vs_dense": 1.205, "training_throughput_vs_dense": 1.219,
+    "energy_per_token_vs_dense": 0.83, "peak_memory_vs_dense": "<0.76",
+    "hardware": "NVIDIA H100", "scope": "end-to-end language models (0.5B-2B parameters, >99% FFN sparsity)",
+    "source": "Sparser, Faster, Lighter Transformer Language Models - Resumo Tecnico, 4 Resultados",
+}
 
 
 def _peaks():
@@ -124,17 +139,28 @@ def oracle_step(inp: syn.FFNInputs, S: int):
     oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, L1)
 
 
-def oracle_rate(inp: syn.FFNInputs, budget_s: float):
+def _omp_set_threads(n: int) -> None:
+    """Sets the OpenMP thread count of this process (the oracle's parallel loops)."""
+    for name in ("libgomp.so.1", "libgomp.so"):
+        try:
+            ctypes.CDLL(name).omp_set_num_threads(int(n))
+            return
+        except OSError:
+            continue
+
+
+def oracle_rate(inp: syn.FFNInputs, budget_s: float, one_core_s: float = 6.0):
     """Tokens/s of the oracle on a sample of the workload sized to take about budget_s:
-    the first S tokens (S from a 32-token probe, at most the whole batch), repeated
-    until budget_s has passed."""
+    the first S tokens (S from an 8-token probe, at most the whole batch), repeated
+    until budget_s has passed; then the same on one core for about one_core_s."""
     import oracle
     oracle.build()
-    S0 = 32
+    cores = oracle.num_threads()
+    S0 = 8
     t0 = time.perf_counter()
     oracle_step(inp, S0)
     t_probe = time.perf_counter() - t0
-    S = int(max(1, min(inp.M, S0 * budget_s / max(t_probe, 1e-3))))
+    S = int(max(1, min(inp.M, S0 * budget_s / 2 / max(t_probe, 1e-3))))
     done, t0 = 0, time.perf_counter()
     while True:
         oracle_step(inp, S)
@@ -142,7 +168,23 @@ def oracle_rate(inp: syn.FFNInputs, budget_s: float):
         dt = time.perf_counter() - t0
         if dt >= budget_s:
             break
-    return done / dt, S, dt, oracle.num_threads(), done
+    one = None
+    if one_core_s > 0:
+        _omp_set_threads(1)
+        try:
+            if oracle.num_threads() == 1:
+                S1 = 2
+                n1, t1 = 0, time.perf_counter()
+                while True:
+                    oracle_step(inp, S1)
+                    n1 += S1
+                    d1 = time.perf_counter() - t1
+                    if d1 >= one_core_s:
+                        break
+                one = {"value": n1 / d1, "tokens": n1, "seconds": d1}
+        finally:
+            _omp_set_threads(cores)
+    return done / dt, S, dt, cores, done, one
 
 
 def max_over_ranks(value: float, world: int) -> float:
@@ -169,11 +211,11 @@ def run_reference(args, rank: int, world: int):
     inp = syn.config_inputs(CONFIG_NAME, with_dy=True)
     total_budget = 150.0
     per_step = total_budget / max(1, args.steps + args.warmup)
-    # size the per-step sample from a 32-token probe
+    # size the per-step sample from an 8-token probe
     t0 = time.perf_counter()
-    oracle_step(inp, 32)
+    oracle_step(inp, 8)
     t_probe = time.perf_counter() - t0
-    S = int(max(1, min(inp.M, 32 * per_step / max(t_probe, 1e-3))))
+    S = int(max(1, min(inp.M, 8 * per_step / max(t_probe, 1e-3))))
     for _ in range(args.warmup):
         oracle_step(inp, S)
     times = []
@@ -203,27 +245,40 @@ def dev16(a: np.ndarray) -> torch.Tensor:
 
 
 class Layer:
-    def __init__(self, inp: syn.FFNInputs):
+    """Device buffers of one workload and the three stages of a step."""
+
+    def __init__(self, inp: syn.FFNInputs, l1: float, cap: int | None = None, sparse: bool = True):
         import activation_sparse_transformer_tcgen05_gb300 as tw
         self.tw = tw
         self.inp = inp
+        self.l1 = l1
         M, d, F, T = inp.M, inp.d, inp.F, inp.T
-        self.x, self.Wu, self.Wd, self.dy = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_down), dev16(inp.dy)
+        self.x, self.Wu, self.Wd = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_down)
+        self.dy = dev16(inp.dy) if inp.dy is not None else None
         self.b = torch.from_numpy(inp.b).cuda()
-        self.cap = M * F
+        self.st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.ws_b = None
+        if not sparse:  # inputs only (the dense layer brings its own buffers)
+            return
+        # slot capacity: M x 256 is ~1.3x the widest 128-row tile at 1 % density
+        # on these shapes (a tile wider than that reports a capacity error)
+        self.cap = cap if cap is not None else M * min(F, 256)
         self.buf = tw.TwellBuffers(M, F, T, self.cap)
         self.y = torch.empty(M, d, dtype=torch.int16, device="cuda")
         # epilogue staging of 32 entries per (row, 256-column block): ~13x the
         # mean count at 1 % density (the full 256 would be as large as an fp32 h)
         self.ws_f = torch.empty(tw.twell_fwd_workspace_bytes(M, d, F, T, self.cap, STAGE_CAP), dtype=torch.uint8,
                                 device="cuda")
+
+    def alloc_bwd(self):
+        tw, inp = self.tw, self.inp
+        M, d, F, T = inp.M, inp.d, inp.F, inp.T
         self.ws_b = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, self.cap), dtype=torch.uint8,
                                 device="cuda")
         self.dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
         self.dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
         self.dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
         self.db = torch.empty(F, dtype=torch.float32, device="cuda")
-        self.st = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def up(self):
         self.tw.twell_up_pack(self.x, self.Wu, None, self.b, self.inp.T, self.buf, self.ws_f, self.st)
@@ -231,9 +286,53 @@ class Layer:
     def down(self):
         self.tw.twell_spmm_down(self.buf, self.Wd, self.y, self.st)
 
+    def fwd(self):
+        self.tw.twell_ffn_fwd(self.x, self.Wu, None, self.b, self.Wd, self.inp.T, self.buf, self.y, self.ws_f,
+                              self.st)
+
     def bwd(self):
-        self.tw.twell_ffn_bwd(self.x, self.Wu, self.Wd, self.buf, self.dy, L1, self.dx, self.dWu, self.dWd,
+        self.tw.twell_ffn_bwd(self.x, self.Wu, self.Wd, self.buf, self.dy, self.l1, self.dx, self.dWu, self.dWd,
                               self.db, self.ws_b, self.st)
+
+    def check(self, where: str):
+        code = self.tw.twell_check(self.st)
+        if code != 0:
+            raise RuntimeError(f"{where}: device status {code}: {self.tw.twell_status_string(code)}")
+
+
+class DenseLayer:
+    """The same layer computed densely with this build's tcgen05 GEMMs (forward and backward)."""
+
+    def __init__(self, L: Layer):
+        tw, inp = L.tw, L.inp
+        M, d, F = inp.M, inp.d, inp.F
+        self.L, self.tw = L, tw
+        self.h = torch.empty(M, F, dtype=torch.int16, device="cuda")
+        self.y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+        self.ws = None
+
+    def alloc_bwd(self):
+        inp = self.L.inp
+        M, d, F = inp.M, inp.d, inp.F
+        self.ws = torch.empty(self.tw.twell_dense_bwd_workspace_bytes(M, d, F), dtype=torch.uint8, device="cuda")
+        self.dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+        self.dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+        self.dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+        self.db = torch.empty(F, dtype=torch.float32, device="cuda")
+
+    def fwd(self):
+        L = self.L
+        self.tw.twell_dense_ffn_fwd(L.x, L.Wu, L.b, L.Wd, self.h, self.y, L.st)
+
+    def bwd(self):
+        L = self.L
+        self.tw.twell_dense_ffn_bwd(L.x, L.Wu, L.Wd, self.h, L.dy, L.l1, self.dx, self.dWu, self.dWd, self.db,
+                                    self.ws, L.st)
+
+    def free(self):
+        for k in ("h", "y", "ws", "dx", "dWu", "dWd", "db"):
+            if hasattr(self, k):
+                setattr(self, k, None)
 
 
 SITES = {1: "up_gemm", 2: "spmm_down", 3: "sddmm", 4: "dx", 5: "csc", 6: "wgrad"}
@@ -241,6 +340,104 @@ SITES = {1: "up_gemm", 2: "spmm_down", 3: "sddmm", 4: "dx", 5: "csc", 6: "wgrad"
 # another site's: their event time spans that overlap, so they never count as
 # the dominant kernel.
 CONCURRENT_SITES = {5: "sddmm"}
+
+
+# ------------------------------------------------------------------ probes --
+
+PROBE_SRC = os.path.join(ROOT, "probes.cu")
+PROBE_LIB = os.path.join(ROOT, "_build", "libprobes.so")
+
+
+def build_probes() -> str:
+    """Compiles probes.cu (FMA and gather ceilings of this benchmark) for sm_103a."""
+    if os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) >= os.path.getmtime(PROBE_SRC):
+        return PROBE_LIB
+    os.makedirs(os.path.dirname(PROBE_LIB), exist_ok=True)
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    tmp = PROBE_LIB + f".tmp{os.getpid()}"
+    subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
+                           "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared", "-o", tmp, PROBE_SRC])
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
+
+
+_probes = None
+
+
+def load_probes():
+    global _probes
+    if _probes is None:
+        lib = ctypes.CDLL(build_probes())
+        P, I = ctypes.c_void_p, ctypes.c_int
+        lib.probe_fma.restype = I
+        lib.probe_fma.argtypes = [I, I, I, P, P]
+        lib.probe_gather.restype = I
+        lib.probe_gather.argtypes = [I, P, I, I, P, I, I, P, P, P]
+        _probes = lib
+    return _probes
+
+
+def fma_peak(stream, sm_count: int):
+    """Measured FP32 FMA rate (TFLOP/s), best of 5: fmaf and the mixed bf16 x bf16 + fp32 form."""
+    lib = load_probes()
+    sink = torch.empty(sm_count * 8 * 256, dtype=torch.float32, device="cuda")
+    blocks, iters = sm_count * 8, 4096
+    out = {}
+    for mode, name in ((0, "fp32_fma"), (1, "bf16_mixed_fma")):
+        best = 0.0
+        for rep in range(6):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            if lib.probe_fma(mode, blocks, iters, ctypes.c_void_p(sink.data_ptr()),
+                             ctypes.c_void_p(stream.cuda_stream)) != 0:
+                raise RuntimeError("probe_fma failed")
+            b.record(stream)
+            torch.cuda.synchronize()
+            if rep:
+                flops = 2.0 * 8 * 16 * iters * blocks * 256
+                best = max(best, flops / (a.elapsed_time(b) * 1e-3) / 1e12)
+        out[name] = best
+    return out
+
+
+def gather_ceiling(W, nnz_per_row: int, reps: int = 6):
+    """Measured rate (TB/s) at which 512-byte stretches of random rows of W
+    (L2-resident) reach the SMs: four forms (128-bit loads with 4 or 8 in flight
+    per lane; bulk copies into shared memory with 3 or 6 batches in flight per
+    warp), best of `reps` each after warm-up."""
+    lib = load_probes()
+    F, d = W.shape
+    rows = 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    idx = torch.randint(0, F, (rows, nnz_per_row), dtype=torch.int32, device="cuda", generator=g)
+    sink = torch.empty(rows * ((d + 255) // 256), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    out = {}
+    for mode, name in ((0, "ldg4"), (1, "ldg8"), (2, "bulk3"), (3, "bulk6")):
+        def call():
+            rc = lib.probe_gather(mode, ctypes.c_void_p(W.data_ptr()), F, d, ctypes.c_void_p(idx.data_ptr()), rows,
+                                  nnz_per_row, ctypes.c_void_p(sink.data_ptr()), ctypes.c_void_p(st.data_ptr()),
+                                  ctypes.c_void_p(stream.cuda_stream))
+            if rc != 0:
+                raise RuntimeError(f"probe_gather mode {mode} failed ({rc})")
+        for _ in range(3):
+            call()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError("probe_gather: a bounded wait gave up")
+        best = min(a.elapsed_time(b) for a, b in ts) * 1e-3
+        out[name] = rows * nnz_per_row * d * 2 / best / 1e12
+    out["best"] = max(out.values())
+    return out
 
 
 class PowerSampler:
@@ -320,30 +517,19 @@ def energy_leg(tw, local_rank: int, runs: dict, tokens: int, seconds: float = 2.
     return out
 
 
-def fp32_peak_tflops(sm_count: int, sm_mhz: float) -> float:
-    """FP32 FMA peak from unit counts and clock: SMs x 128 FMA/clk x 2 FLOP x clock."""
-    return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
-
-
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
-# call site's kernel on this workload, from one `ncu --set full` capture, with
-# the SHA-256 of the source file it was built from: once that file changes the
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# each call site's kernel, from one ncu capture per (workload, site), with the
+# SHA-256 of the source file it was built from: once that file changes the
 # figure no longer describes the kernel and the site reports traffic null.
 NCU_TRAFFIC = {
-    1: ("twell_gemm.cu", "26dfe7157735f1512e423b5748429ec2141ba9124d9bd14beb4892b356f8ab92", 52.946176e6),
-    2: ("twell_sparse.cu", "4b7c58e6176bed50c54b847161a48419ff7d3065e044164f018d213fcae6c6bf", 37.770496e6),
-    3: ("twell_sparse.cu", "4b7c58e6176bed50c54b847161a48419ff7d3065e044164f018d213fcae6c6bf", 52.641792e6),
-    4: ("twell_sparse.cu", "4b7c58e6176bed50c54b847161a48419ff7d3065e044164f018d213fcae6c6bf", 38.832384e6),
-    6: ("twell_sparse.cu", "4b7c58e6176bed50c54b847161a48419ff7d3065e044164f018d213fcae6c6bf", 133.058816e6),
 }
 
 
 def ncu_traffic(site: int, workload: str):
-    ent = NCU_TRAFFIC.get(site)
-    if ent is None or workload != CONFIG_NAME:
+    ent = NCU_TRAFFIC.get((workload, site))
+    if ent is None:
         return None
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "activation_sparse_transformer_tcgen05_gb300",
-                        "csrc", ent[0])
+    path = os.path.join(ROOT, "activation_sparse_transformer_tcgen05_gb300", "csrc", ent[0])
     try:
         with open(path, "rb") as f:
             digest = hashlib.sha256(f.read()).hexdigest()
@@ -352,66 +538,64 @@ def ncu_traffic(site: int, workload: str):
     return ent[2] if digest == ent[1] else None
 
 
-def kernel_roofline(site: int, us: float, inp, slots: int, nnz: int, peaks, fp32_peak: float):
-    """Roofline of one kernel call site: bound, achieved, peak, unit, frac (traffic filled from ncu)."""
-    M, d, F = inp.M, inp.d, inp.F
-    s = us * 1e-6
-    if site == 1:
-        flops = 2.0 * M * d * F
-        a = flops / s / 1e12
-        return {"bound": "tensor", "achieved": a, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                "frac": a / peaks["bf16"], "traffic": ncu_traffic(site, CONFIG_NAME),
-                "algorithmic": f"{flops / 1e9:.1f} GFLOP"}
-    if site == 5:
-        by = slots * (4 + 2 + 4) + nnz * (4 + 2 + 4 + 8) + F * 8
-        a = by / s / 1e9
-        return {"bound": "hbm", "achieved": a, "peak": peaks["hbm"], "unit": "GB/s", "frac": a / peaks["hbm"],
-                "traffic": None, "algorithmic": f"{by / 1e6:.1f} MB"}
-    flops = 2.0 * nnz * d * (2 if site == 6 else 1)
-    a = flops / s / 1e12
-    return {"bound": "alu", "achieved": a, "peak": fp32_peak, "unit": "TFLOP/s", "frac": a / fp32_peak,
-            "traffic": ncu_traffic(site, CONFIG_NAME),
-            "algorithmic": f"{flops / 1e9:.2f} GFLOP fp32 FMA on stored entries"}
-
-
-# Bytes each gather kernel pulls through L2 per stored entry, in rows of d bf16:
+# Rows of d bf16 each sparse kernel pulls through L2 per stored entry:
 # down-projection and SDDMM a W_down row, dx a W_up row, weight gradients an x
 # row and a dy row.
 GATHER_ROWS = {2: 1, 3: 1, 4: 1, 6: 2}
 
 
-def gather_ceiling(tw, W, nnz_per_row: int, reps: int = 10):
-    """Measured rate (TB/s) of the sparse kernels' access pattern alone: warps
-    gathering 512-byte stretches of random rows of W (L2-resident) with
-    128-bit loads (twell_gather_probe), best of `reps` after warm-up."""
-    F, d = W.shape
-    rows = 4096
-    g = torch.Generator(device="cuda")
-    g.manual_seed(0)
-    idx = torch.randint(0, F, (rows, nnz_per_row), dtype=torch.int32, device="cuda", generator=g)
-    sink = torch.empty(rows * ((d + 255) // 256), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
-    for _ in range(3):
-        tw.twell_gather_probe(W, idx, sink)
-    ts = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        tw.twell_gather_probe(W, idx, sink)
-        b.record(stream)
-        ts.append((a, b))
-    torch.cuda.synchronize()
-    best = min(a.elapsed_time(b) for a, b in ts) * 1e-3
-    return rows * nnz_per_row * d * 2 / best / 1e12
+def site_work(site: int, inp, slots: int, nnz: int):
+    """(flops, compulsory bytes) of one launch of a call site: every input read
+    once, every output written once (the roofline's algorithmic work)."""
+    M, d, F = inp.M, inp.d, inp.F
+    if site == 1:  # up GEMM + TwELL epilogue: x, W_up in; staged entries out
+        return 2.0 * M * d * F, M * d * 2 + F * d * 2 + nnz * 4 + F * 4
+    if site == 2:  # y = TwELL W_down
+        return 2.0 * nnz * d, F * d * 2 + slots * 6 + M * d * 2
+    if site == 3:  # dpre on the stored slots
+        return 2.0 * nnz * d, M * d * 2 + F * d * 2 + slots * 4 + slots * 4
+    if site == 4:  # dx = dpre W_up
+        return 2.0 * nnz * d, F * d * 2 + slots * 8 + M * d * 2
+    if site == 5:  # column lists: masks, counts, pointers (TwELL indices only)
+        rb = (M + 63) // 64
+        return 0.0, slots * 4 + M * 4 + rb * F * (8 + 4) * 2 + F * 8
+    if site == 6:  # dW_up, dW_down, db from the column lists
+        return 4.0 * nnz * d, 2 * M * d * 2 + nnz * 10 + 2 * F * d * 4 + F * 4
+    raise ValueError(site)
 
 
-def gather_roofline(site: int, us: float, nnz: int, d: int, ceiling_tbs: float):
-    if site not in GATHER_ROWS:
-        return None
-    by = GATHER_ROWS[site] * nnz * d * 2
-    a = by / (us * 1e-6) / 1e12
-    return {"achieved_TBs": a, "ceiling_TBs": ceiling_tbs, "frac": a / ceiling_tbs,
-            "bytes_gathered": by, "ceiling_source": "twell_gather_probe, same run"}
+def kernel_roofline(site: int, us: float, inp, slots: int, nnz: int, peaks, ceil: dict, workload: str):
+    """Roofline of one call site. tensor-bound: FLOPs at the bf16 peak. CUDA-core
+    gathers: the slower of compulsory bytes at the HBM peak and FLOPs at the
+    measured FP32 FMA peak ("alu"), plus the HBM-only fraction the north-star
+    target is stated in, the most that fraction can be when the FMAs run at
+    peak, and the gathered bytes against the measured gather ceiling."""
+    s = us * 1e-6
+    flops, byts = site_work(site, inp, slots, nnz)
+    hbm = peaks["hbm"] * 1e9
+    if site == 1:
+        a = flops / s / 1e12
+        return {"bound": "tensor", "achieved": a, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": a / peaks["bf16"], "traffic": ncu_traffic(site, workload),
+                "algorithmic": f"{flops / 1e9:.1f} GFLOP (2 M d_model d_ff)", "hbm_frac": byts / s / hbm}
+    if site == 5:
+        a = byts / s / 1e9
+        return {"bound": "hbm", "achieved": a, "peak": peaks["hbm"], "unit": "GB/s", "frac": a / peaks["hbm"],
+                "traffic": None, "algorithmic": f"{byts / 1e6:.1f} MB"}
+    fma = ceil["fma_tflops"] * 1e12
+    t_roof = max(byts / hbm, flops / fma)
+    a = flops / s / 1e12
+    out = {"bound": "alu", "achieved": a, "peak": ceil["fma_tflops"], "unit": "TFLOP/s", "frac": a / ceil["fma_tflops"],
+           "traffic": ncu_traffic(site, workload),
+           "algorithmic": f"{flops / 1e9:.2f} GFLOP of fp32 FMAs on the stored entries; {byts / 1e6:.0f} MB compulsory",
+           "roofline_frac": t_roof / s,
+           "hbm_frac": byts / s / hbm,
+           "hbm_frac_at_fma_peak": min(1.0, (byts / hbm) / (flops / fma))}
+    if site in GATHER_ROWS and ceil.get("gather_tbs"):
+        by = GATHER_ROWS[site] * nnz * inp.d * 2
+        out["l2_gather"] = {"bytes": by, "achieved_TBs": by / s / 1e12, "ceiling_TBs": ceil["gather_tbs"],
+                            "frac": by / s / 1e12 / ceil["gather_tbs"]}
+    return out
 
 
 def stage_roofline(name, ms, inp, slots, nnz, peaks):
@@ -421,17 +605,15 @@ def stage_roofline(name, ms, inp, slots, nnz, peaks):
         flops = 2.0 * M * d * F
         a = flops / s / 1e12
         return {"bound": "tensor", "achieved": a, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                "frac": a / peaks["bf16"], "traffic": None,
-                "algorithmic": f"{flops / 1e9:.1f} GFLOP (2 M d_model d_ff)"}
+                "frac": a / peaks["bf16"], "algorithmic": f"{flops / 1e9:.1f} GFLOP (2 M d_model d_ff)"}
     if name == "spmm_down":
-        # compulsory: W_down once, the TwELL (idx + val) once, y written once
-        by = F * d * 2 + slots * 6 + M * d * 2 + M * 4
+        by = F * d * 2 + slots * 6 + M * d * 2
     else:
         # compulsory: x, dy, W_up, W_down, TwELL read once; dx, dW_up, dW_down, db written once
         by = 2 * M * d * 2 + 2 * F * d * 2 + slots * 6 + M * d * 2 + 2 * F * d * 4 + F * 4
     a = by / s / 1e9
     return {"bound": "hbm", "achieved": a, "peak": peaks["hbm"], "unit": "GB/s", "frac": a / peaks["hbm"],
-            "traffic": None, "algorithmic": f"{by / 1e6:.1f} MB compulsory"}
+            "algorithmic": f"{by / 1e6:.1f} MB compulsory"}
 
 
 class L2Flush:
@@ -562,20 +744,38 @@ def down_variants(tw, buf, Wd, y, st, flush, stream, reps: int = 5):
             "rows_over_union_tc": rows_us / tc_us}
 
 
+def timed_ms(fn, flush, stream, st, tw, n: int = 5, warm: int = 2):
+    """Median time (ms) of fn(), L2 flushed before each call."""
+    evs = []
+    for i in range(n + warm):
+        flush.fill_(i & 0xff)
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b2.record(stream)
+        if i >= warm:
+            evs.append((a, b2))
+    torch.cuda.synchronize()
+    code = tw.twell_check(st)
+    if code != 0:
+        raise RuntimeError(f"device status {code}: {tw.twell_status_string(code)}")
+    return statistics.median(a.elapsed_time(b2) for a, b2 in evs)
+
+
+SWEEP_NAMES = ("sweep90", "sweep99", "sweep999", "sweep90s", "sweep99s", "sweep999s")
+
+
 def hybrid_leg(tw, flush, stream, reps: int = 5):
-    """The skewed sweep workloads (8192 tokens, d_model 4096, d_ff 16384, x rows
-    scaled by LogNormal(0, 1), gate biases for nominal 90 / 99 / 99.9 %
-    sparsity): forward and backward time and memory of plain TwELL, of the
-    hybrid ELL + dense-overflow format (C = 1.25 % of d_ff) and of the dense
-    layer (forward measured; training step estimated as 3 x the forward)."""
-    inp = syn.config_inputs("sweep90")  # the three differ only in the bias
+    """The sparsity/skew sweep (8192 tokens, d_model 4096, d_ff 16384, x rows
+    scaled by LogNormal(0, 1); biases for 90 / 99 / 99.9 % sparsity, nominal and
+    skew-corrected): forward and fwd + bwd time and memory of plain TwELL, of
+    the hybrid ELL + dense-overflow format (C = 1.25 % of d_ff), and of the
+    dense layer (this build's tcgen05 GEMMs, forward and backward measured)."""
+    inp = syn.config_inputs("sweep90", with_dy=True)  # the six differ only in the bias
     M, d, F, T = inp.M, inp.d, inp.F, inp.T
-    x, Wu, Wd = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_down)
+    x, Wu, Wd, dy = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_down), dev16(inp.dy)
     WdT = Wd.view(F, d).t().contiguous()
     WuT = Wu.view(F, d).t().contiguous()
-    g = torch.Generator(device="cuda")
-    g.manual_seed(0)
-    dy = torch.randn(M, d, device="cuda", generator=g).to(torch.bfloat16).view(torch.int16)
     C = round(HYBRID_C_FRAC * F)
     l1 = 1e-4
     y = torch.empty(M, d, dtype=torch.int16, device="cuda")
@@ -586,22 +786,13 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def timed(fn, n=reps):
-        evs = []
-        for i in range(n + 2):
-            flush.fill_(i & 0xff)
-            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b2.record(stream)
-            if i >= 2:
-                evs.append((a, b2))
-        torch.cuda.synchronize()
-        if tw.twell_check(st) != 0:
-            raise RuntimeError(f"hybrid leg: device status {tw.twell_check(st)}")
-        return statistics.median(a.elapsed_time(b2) for a, b2 in evs)
+        return timed_ms(fn, flush, stream, st, tw, n=n)
 
-    out = {"C": C, "workload": "M=8192, d_model=4096, d_ff=16384, T=128, x rows x LogNormal(0,1), l1=1e-4"}
-    for name in ("sweep90", "sweep99", "sweep999"):
+    # the dense layer does not depend on the sparsity: one measurement per bias
+    # only differs in the ReLU mask (its GEMMs do the same work)
+    out = {"C": C, "workload": "M=8192, d_model=4096, d_ff=16384, T=128, x rows x LogNormal(0,1), l1=1e-4",
+           "targets": {n: syn.SWEEP_TARGETS[n] for n in SWEEP_NAMES}}
+    for name in SWEEP_NAMES:
         b = torch.full((F,), float(syn.CONFIGS[name]["bias"]), dtype=torch.float32, device="cuda")
         buf = tw.TwellBuffers(M, F, T, M * F)
         ws = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_FWD, M, d, F, T, M * F), dtype=torch.uint8,
@@ -610,7 +801,7 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
         slots, nnz = buf.slots(), int(buf.nnz.sum().item())
         del ws
         down = down_variants(tw, buf, Wd, y, st, flush, stream)
-        wsb = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, M * F), dtype=torch.uint8,
+        wsb = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, max(slots, 1)), dtype=torch.uint8,
                           device="cuda")
         ms_tw_b = timed(lambda: tw.twell_ffn_bwd(x, Wu, Wd, buf, dy, l1, dx, dWu, dWd, db, wsb, st), n=2)
         del buf, wsb
@@ -626,86 +817,92 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
         ms_h_b = timed(lambda: tw.twell_hybrid_ffn_bwd(x, Wu, Wd, WuT, hb, ov, dy, l1, dx, dWu, dWd, db, wshb, st))
         del hb, ov, wshb
         hd = torch.empty(M, F, dtype=torch.int16, device="cuda")
-        ms_d = timed(lambda: tw.twell_dense_ffn_fwd(x, Wu, b, WdT, hd, y, st))
-        del hd
-        out[name] = {"density": nnz / (M * F), "twell_ms": ms_tw, "hybrid_ms": ms_h, "dense_ms": ms_d,
-                     "twell_bwd_ms": ms_tw_b, "hybrid_bwd_ms": ms_h_b,
-                     "twell_step_ms": ms_tw + ms_tw_b, "hybrid_step_ms": ms_h + ms_h_b,
-                     "dense_step_estimate_ms": 3 * ms_d,
+        wsd = torch.empty(tw.twell_dense_bwd_workspace_bytes(M, d, F), dtype=torch.uint8, device="cuda")
+        ms_d = timed(lambda: tw.twell_dense_ffn_fwd(x, Wu, b, Wd, hd, y, st))
+        ms_d_b = timed(lambda: tw.twell_dense_ffn_bwd(x, Wu, Wd, hd, dy, l1, dx, dWu, dWd, db, wsd, st))
+        del hd, wsd
+        best = min(ms_tw + ms_tw_b, ms_h + ms_h_b)
+        out[name] = {"bias": syn.CONFIGS[name]["bias"], "density": nnz / (M * F), "padding_ratio": slots / max(nnz, 1),
+                     "twell_ms": ms_tw, "hybrid_ms": ms_h, "dense_ms": ms_d,
+                     "twell_bwd_ms": ms_tw_b, "hybrid_bwd_ms": ms_h_b, "dense_bwd_ms": ms_d_b,
+                     "twell_step_ms": ms_tw + ms_tw_b, "hybrid_step_ms": ms_h + ms_h_b, "dense_step_ms": ms_d + ms_d_b,
+                     "best_sparse_step_vs_dense_step": (ms_d + ms_d_b) / best,
                      "twell_MB": slots * 6 / 1e6, "hybrid_MB": (ell_slots * 6 + n_ov * F * 2) / 1e6,
+                     "dense_h_MB": M * F * 2 / 1e6,
                      "overflow_rows": n_ov, "hybrid_vs_twell": ms_tw / ms_h, "hybrid_vs_dense": ms_d / ms_h,
                      "hybrid_step_vs_twell_step": (ms_tw + ms_tw_b) / (ms_h + ms_h_b),
                      "down_projection": down}
     return out
 
 
-def training_leg(tw, flush, stream, reps: int = 5):
-    """The training workload (16384 tokens, d_model 4096, d_ff 16384, ReLU, bias
-    -2.33, L1 1e-4): one fwd + bwd step through the library, L2 flushed before
-    each, and the dense tcgen05 forward on the same shape. Inputs are drawn on
-    the device (seeded; the distributions of the synthetic generator)."""
-    c = syn.CONFIGS["training"]
-    M, d, F, T = c["M"], c["d"], c["F"], c["T"]
-    g = torch.Generator(device="cuda")
-    g.manual_seed(0)
+def inference_leg(tw, flush, stream, peaks, reps: int = 20):
+    """The inference workload's forward (4096 tokens, d_model 2048, d_ff 8192,
+    ~99 % sparse, TwELL tile 128): twell_ffn_fwd against this build's dense
+    tcgen05 forward, L2 flushed before each call."""
+    inp = syn.config_inputs("inference")
+    L = Layer(inp, 0.0)
+    D = DenseLayer(L)
+    ms = timed_ms(L.fwd, flush, stream, L.st, tw, n=reps)
+    ms_d = timed_ms(D.fwd, flush, stream, L.st, tw, n=reps)
+    nnz = int(L.buf.nnz.sum().item())
+    up_flops = 2.0 * inp.M * inp.d * inp.F
+    out = {"workload": "M=4096, d_model=2048, d_ff=8192, T=128, bias=-2.33, forward only",
+           "tokens_per_s": inp.M / (ms / 1000.0), "ms": ms, "density": nnz / (inp.M * inp.F),
+           "dense_tcgen05_fwd_ms": ms_d, "dense_tokens_per_s": inp.M / (ms_d / 1000.0),
+           "sparse_vs_dense": ms_d / ms,
+           "up_gemm_tensor_frac_if_alone": None}
+    del L, D
+    return out, up_flops
 
-    def bf(shape, scale):
-        return (torch.randn(shape, device="cuda", generator=g) * scale).to(torch.bfloat16).view(torch.int16)
 
-    x, dy = bf((M, d), 1.0), bf((M, d), 1.0)
-    Wu, Wd = bf((F, d), d ** -0.5), bf((F, d), F ** -0.5)
-    b = torch.full((F,), float(c["bias"]), dtype=torch.float32, device="cuda")
-    cap = M * 256  # slot capacity: ~1.3x the expected width at 1 % density
-    buf = tw.TwellBuffers(M, F, T, cap)
-    ws_f = torch.empty(tw.twell_fwd_workspace_bytes(M, d, F, T, cap, STAGE_CAP), dtype=torch.uint8, device="cuda")
-    ws_b = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, cap), dtype=torch.uint8, device="cuda")
-    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
-    dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
-    dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
-    dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
-    db = torch.empty(F, dtype=torch.float32, device="cuda")
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    evs = []
-    for i in range(reps + 2):
-        flush.fill_(i & 0xff)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record(stream)
-        tw.twell_ffn_fwd(x, Wu, None, b, Wd, T, buf, y, ws_f, st)
-        e[1].record(stream)
-        tw.twell_ffn_bwd(x, Wu, Wd, buf, dy, float(c["l1"]), dx, dWu, dWd, db, ws_b, st)
-        e[2].record(stream)
-        if i >= 2:
-            evs.append(e)
+def training_memory_leg(tw, inp, l1: float):
+    """Peak device memory (torch.cuda.max_memory_allocated) of one training
+    step, sparse against dense, each in a fresh scope: the resident inputs and
+    weights (x, dy, W_up, W_down, b), then everything the step allocates (the
+    TwELL sized for the workload, the forward's and backward's workspaces,
+    y, dx and the fp32 weight gradients; for the dense layer the dense h, its
+    backward's workspace and the same outputs)."""
+    out = {}
+    for kind in ("twell", "dense"):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        L = Layer(inp, l1, sparse=False)
+        resident = torch.cuda.memory_allocated() - base
+        if kind == "twell":
+            M, d, F, T = inp.M, inp.d, inp.F, inp.T
+            L.cap = M * min(F, 256)
+            L.buf = tw.TwellBuffers(M, F, T, L.cap)
+            L.y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+            L.ws_f = torch.empty(tw.twell_fwd_workspace_bytes(M, d, F, T, L.cap, STAGE_CAP), dtype=torch.uint8,
+                                 device="cuda")
+            L.fwd()
+            torch.cuda.synchronize()
+            L.ws_f = None  # the forward's staging is transient
+            L.alloc_bwd()
+            L.bwd()
+        else:
+            D = DenseLayer(L)
+            D.fwd()
+            D.alloc_bwd()
+            D.bwd()
+        torch.cuda.synchronize()
+        L.check(f"memory leg ({kind})")
+        peak = torch.cuda.max_memory_allocated() - base
+        out[kind] = {"peak_MB": peak / 1e6, "resident_inputs_MB": resident / 1e6,
+                     "step_MB": (peak - resident) / 1e6}
+        del L
+        if kind == "dense":
+            del D
     torch.cuda.synchronize()
-    code = tw.twell_check(st)
-    if code != 0:
-        raise RuntimeError(f"training leg: device status {code}: {tw.twell_status_string(code)}")
-    fwd = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
-    bwd = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
-    nnz = int(buf.nnz.sum().item())
-    del ws_b, dWu, dWd
-    down = down_variants(tw, buf, Wd, y, st, flush, stream)
-    WdT = Wd.view(F, d).t().contiguous()
-    hd = torch.empty(M, F, dtype=torch.int16, device="cuda")
-    dts = []
-    for i in range(reps + 2):
-        flush.fill_(i & 0xff)
-        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        tw.twell_dense_ffn_fwd(x, Wu, b, WdT, hd, y, st)
-        b2.record(stream)
-        if i >= 2:
-            dts.append((a, b2))
-    torch.cuda.synchronize()
-    dense_fwd = statistics.median(a.elapsed_time(b2) for a, b2 in dts)
-    return {"workload": f"M={M}, d_model={d}, d_ff={F}, T={T}, bias={c['bias']}, l1={c['l1']}",
-            "density": nnz / (M * F), "fwd_ms": fwd, "bwd_ms": bwd, "step_ms": fwd + bwd,
-            "tokens_per_s": M / ((fwd + bwd) / 1000.0), "dense_fwd_ms": dense_fwd,
-            "dense_step_estimate_ms": 3 * dense_fwd, "down_projection": down,
-            "dense_step_note": "3 x the measured dense forward: a dense backward runs each forward GEMM shape twice"}
+    torch.cuda.empty_cache()
+    out["twell_over_dense_peak"] = out["twell"]["peak_MB"] / out["dense"]["peak_MB"]
+    out["twell_over_dense_step"] = out["twell"]["step_MB"] / out["dense"]["step_MB"]
+    return out
 
 
-EXTRA_LEGS = ("e2e", "dense", "energy", "down", "decode", "hybrid", "training")
+EXTRA_LEGS = ("e2e", "dense", "inference", "energy", "memory", "down", "decode", "hybrid")
 
 
 def dominant_site(site_us: dict) -> int:
@@ -719,6 +916,59 @@ def leg_on(args, name: str) -> bool:
     return args.legs == "all" or name in args.legs.split(",")
 
 
+def e2e_leg(tw, L: Layer, inp, flush, stream, steps: int, world: int):
+    """The step through the public API with host buffers: every step copies x
+    and dy in from pinned host memory and y and dx out, inside the timed region.
+    dy (needed only by the backward) comes in, and y goes out, on a copy stream
+    while the compute stream works; the step ends when all four copies are done."""
+    xh = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).pin_memory()
+    dyh = torch.from_numpy(np.ascontiguousarray(inp.dy).view(np.int16)).pin_memory()
+    yh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
+    dxh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
+    ke = max(3, min(steps, 30))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
+    cstream = torch.cuda.Stream()
+    bwd_done = torch.cuda.Event()
+    bwd_done.record(stream)
+    for i in range(ke + 3):
+        flush.fill_(i & 0xff)
+        e = evs[i - 3] if i >= 3 else None
+        if e:
+            e[0].record(stream)
+        start = torch.cuda.Event()
+        start.record(stream)
+        L.x.copy_(xh, non_blocking=True)
+        cstream.wait_event(start)
+        cstream.wait_event(bwd_done)  # the previous backward has read dy
+        with torch.cuda.stream(cstream):
+            L.dy.copy_(dyh, non_blocking=True)
+        dy_in = torch.cuda.Event()
+        dy_in.record(cstream)
+        tw.twell_ffn_fwd(L.x, L.Wu, None, L.b, L.Wd, inp.T, L.buf, L.y, L.ws_f, L.st)
+        fwd_done = torch.cuda.Event()
+        fwd_done.record(stream)
+        cstream.wait_event(fwd_done)
+        with torch.cuda.stream(cstream):
+            yh.copy_(L.y, non_blocking=True)
+        y_out = torch.cuda.Event()
+        y_out.record(cstream)
+        stream.wait_event(dy_in)
+        L.bwd()
+        bwd_done = torch.cuda.Event()
+        bwd_done.record(stream)
+        dxh.copy_(L.dx, non_blocking=True)
+        stream.wait_event(y_out)  # the step ends when y has reached the host too
+        if e:
+            e[1].record(stream)
+    torch.cuda.synchronize()
+    L.check("e2e")
+    ems = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return {"value": world * inp.M / (ems / 1000.0), "unit": UNIT,
+            "h2d_bytes_per_step": int(xh.numel() * 2 + dyh.numel() * 2),
+            "d2h_bytes_per_step": int(yh.numel() * 2 + dxh.numel() * 2), "ms_per_step": ems,
+            "api": "twell_ffn_fwd + twell_ffn_bwd"}
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import activation_sparse_transformer_tcgen05_gb300 as tw
     from activation_sparse_transformer_tcgen05_gb300 import build as tbuild
@@ -726,7 +976,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(local_rank)
     peaks = _peaks()
     inp = syn.config_inputs(CONFIG_NAME, with_dy=True)
-    L = Layer(inp)
+    L = Layer(inp, L1)
+    L.alloc_bwd()
     flush = L2Flush(FLUSH_BYTES)
     stream = torch.cuda.current_stream()
 
@@ -742,9 +993,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     for i in range(args.warmup):
         flush.fill_(i & 0xff)
         step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
-    code = tw.twell_check(L.st)
-    if code != 0:
-        raise RuntimeError(f"device status {code}: {tw.twell_status_string(code)}")
+    L.check("warm-up")
     slots = L.buf.slots()
     nnz = int(L.buf.nnz.sum().item())
 
@@ -752,7 +1001,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     site_us = {}
     for site in SITES:
         evs = []
-        for i in range(5):
+        for i in range(4):
             a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             b2.record(stream)
@@ -790,9 +1039,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    code = tw.twell_check(L.st)
-    if code != 0:
-        raise RuntimeError(f"device status {code}: {tw.twell_status_string(code)}")
+    L.check("timed steps")
 
     up = [e[0].elapsed_time(e[1]) for e in events]
     down = [e[1].elapsed_time(e[2]) for e in events]
@@ -802,123 +1049,78 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     value = whole_job_rate(inp.M, world, ms_step)
     ms_fwd = ms["up_pack"] + ms["spmm_down"]
 
+    # ---- measured ceilings of the CUDA-core kernels (probes.cu, same run)
+    sms = tw.twell_device_sm_count()
+    fma = fma_peak(stream, sms)
+    gath = gather_ceiling(L.Wd.view(inp.F, inp.d), max(1, round(nnz / inp.M)))
+    ceil = {"fma_tflops": fma["bf16_mixed_fma"], "gather_tbs": gath["best"]}
+
     stages = {k: dict(ms=v, **stage_roofline(k, v, inp, slots, nnz, peaks)) for k, v in ms.items()}
-    fp32_peak = fp32_peak_tflops(tw.twell_device_sm_count(), peaks["sm_max_mhz"])
     dom_us = statistics.mean(a.elapsed_time(b2) for a, b2 in kev) * 1000.0
-    roof = kernel_roofline(dom_site, dom_us, inp, slots, nnz, peaks, fp32_peak)
-    roof = {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic", "algorithmic")}
+    full = kernel_roofline(dom_site, dom_us, inp, slots, nnz, peaks, ceil, CONFIG_NAME)
+    roof = {k: full[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = SITES[dom_site]
     roof["us_per_launch"] = dom_us
-    roof["peak_source"] = (f"{peaks['src']} (MEASURED_PEAKS.json)" if roof["bound"] != "alu" else
-                           f"derived: {tw.twell_device_sm_count()} SMs x 128 FMA/clk x 2 x {peaks['sm_max_mhz']:.0f} MHz")
-    ceiling = gather_ceiling(tw, L.Wd.view(inp.F, inp.d), max(1, round(nnz / inp.M)))
-    g_dom = gather_roofline(dom_site, dom_us, nnz, inp.d, ceiling)
-    if g_dom:
-        roof["l2_gather"] = g_dom
+    roof["algorithmic"] = full["algorithmic"]
+    roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if roof["bound"] != "alu" else
+                           "measured in this run: probes.cu FP32 FMA probe (fma.rn.f32.bf16, the kernels' form)")
+    for k in ("roofline_frac", "hbm_frac", "hbm_frac_at_fma_peak", "l2_gather"):
+        if k in full:
+            roof[k] = full[k]
     kernels = {}
     for k, v in site_us.items():
-        kr = kernel_roofline(k, v, inp, slots, nnz, peaks, fp32_peak)
-        kernels[SITES[k]] = dict(us=v, **{q: r for q, r in kr.items()
-                                          if q in ("bound", "achieved", "unit", "frac", "traffic")})
-        gk = gather_roofline(k, v, nnz, inp.d, ceiling)
-        if gk:
-            kernels[SITES[k]]["l2_gather_frac"] = gk["frac"]
+        kr = kernel_roofline(k, v, inp, slots, nnz, peaks, ceil, CONFIG_NAME)
+        kernels[SITES[k]] = dict(us=v, **{q: r for q, r in kr.items() if q != "algorithmic"})
         if k in CONCURRENT_SITES:
             kernels[SITES[k]]["concurrent_with"] = CONCURRENT_SITES[k]
 
-    # ---- end to end through the public API with host buffers
-    e2e = None
-    if leg_on(args, "e2e"):
-        xh = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).pin_memory()
-        dyh = torch.from_numpy(np.ascontiguousarray(inp.dy).view(np.int16)).pin_memory()
-        yh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
-        dxh = torch.empty(inp.M, inp.d, dtype=torch.int16).pin_memory()
-        ke = max(3, min(args.steps, 50))
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ke)]
-        # Each step copies x in, runs the forward, copies y out, runs the
-        # backward and copies dx out; dy (needed only by the backward) comes in
-        # and y goes out on a copy stream while the compute stream works.
-        cstream = torch.cuda.Stream()
-        bwd_done = torch.cuda.Event()
-        bwd_done.record(stream)
-        for i in range(ke + 3):
-            flush.fill_(i & 0xff)
-            e = evs[i - 3] if i >= 3 else None
-            if e:
-                e[0].record(stream)
-            start = torch.cuda.Event()
-            start.record(stream)
-            L.x.copy_(xh, non_blocking=True)
-            cstream.wait_event(start)
-            cstream.wait_event(bwd_done)  # the previous backward has read dy
-            with torch.cuda.stream(cstream):
-                L.dy.copy_(dyh, non_blocking=True)
-            dy_in = torch.cuda.Event()
-            dy_in.record(cstream)
-            tw.twell_ffn_fwd(L.x, L.Wu, None, L.b, L.Wd, inp.T, L.buf, L.y, L.ws_f, L.st)
-            fwd_done = torch.cuda.Event()
-            fwd_done.record(stream)
-            cstream.wait_event(fwd_done)
-            with torch.cuda.stream(cstream):
-                yh.copy_(L.y, non_blocking=True)
-            y_out = torch.cuda.Event()
-            y_out.record(cstream)
-            stream.wait_event(dy_in)
-            L.bwd()
-            bwd_done = torch.cuda.Event()
-            bwd_done.record(stream)
-            dxh.copy_(L.dx, non_blocking=True)
-            stream.wait_event(y_out)  # the step ends when y has reached the host too
-            if e:
-                e[1].record(stream)
-        torch.cuda.synchronize()
-        ems = statistics.mean(a.elapsed_time(b) for a, b in evs)
-        e2e = {"value": world * inp.M / (ems / 1000.0), "unit": UNIT,
-               "h2d_bytes_per_step": int(xh.numel() * 2 + dyh.numel() * 2),
-               "d2h_bytes_per_step": int(yh.numel() * 2 + dxh.numel() * 2), "ms_per_step": ems}
+    e2e = e2e_leg(tw, L, inp, flush, stream, args.steps, world) if leg_on(args, "e2e") else None
 
-    # ---- the build's own dense tcgen05 FFN forward on the same workload (context)
-    WdT = L.Wd.view(inp.F, inp.d).t().contiguous()
-    hd = torch.empty(inp.M, inp.F, dtype=torch.int16, device="cuda")
-    dts = []
-    for i in range(13 if leg_on(args, "dense") else 0):
-        flush.fill_(i & 0xff)
-        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        tw.twell_dense_ffn_fwd(L.x, L.Wu, L.b, WdT, hd, L.y, L.st)
-        b2.record(stream)
-        dts.append((a, b2))
-    torch.cuda.synchronize()
-    dense_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in dts[3:]) if dts else None
+    # ---- the same step computed densely with this build's tcgen05 GEMMs
+    dense = None
+    D = None
+    if leg_on(args, "dense"):
+        D = DenseLayer(L)
+        D.alloc_bwd()
+        d_f = timed_ms(D.fwd, flush, stream, L.st, tw, n=8)
+        d_b = timed_ms(D.bwd, flush, stream, L.st, tw, n=8)
+        gemm_flops = 2.0 * inp.M * inp.d * inp.F
+        dense = {"fwd_ms": d_f, "bwd_ms": d_b, "step_ms": d_f + d_b,
+                 "tokens_per_s": world * inp.M / ((d_f + d_b) / 1000.0),
+                 "tensor_frac_of_bf16_sustained": 6 * gemm_flops / ((d_f + d_b) / 1000.0) / 1e12 / peaks["bf16_sust"],
+                 "sparse_step_vs_dense_step": (d_f + d_b) / ms_step,
+                 "sparse_fwd_vs_dense_fwd": d_f / ms_fwd}
 
-    # ---- energy per token and memory, sparse against dense (forward; and the sparse training step)
-    energy, memory = None, None
+    energy = None
     if leg_on(args, "energy"):
-        energy = energy_leg(tw, local_rank, {
-            "twell_fwd": lambda: tw.twell_ffn_fwd(L.x, L.Wu, None, L.b, L.Wd, inp.T, L.buf, L.y, L.ws_f, L.st),
-            "dense_fwd": lambda: tw.twell_dense_ffn_fwd(L.x, L.Wu, L.b, WdT, hd, L.y, L.st),
-            "twell_fwd_bwd": lambda: (L.up(), L.down(), L.bwd()),
-        }, inp.M)
-        if energy.get("twell_fwd") and energy.get("dense_fwd"):
-            energy["dense_over_twell_fwd"] = energy["dense_fwd"]["uJ_per_token"] / energy["twell_fwd"]["uJ_per_token"]
-        memory = {
-            "saved_for_backward_MB": {"twell": (slots * 6 + inp.M * 4 + (inp.M // inp.T + 2) * 12) / 1e6,
-                                      "dense_h_bf16": inp.M * inp.F * 2 / 1e6},
-            "forward_workspace_MB": {"twell": L.ws_f.numel() / 1e6, "twell_stage_cap": STAGE_CAP,
-                                     "dense_h_bf16": inp.M * inp.F * 2 / 1e6},
-            "backward_workspace_MB": {"twell_at_actual_slots": tw.twell_workspace_bytes(
-                tw.OP_FFN_BWD, inp.M, inp.d, inp.F, inp.T, slots) / 1e6},
-        }
-    union = down_variants(tw, L.buf, L.Wd, L.y, L.st, flush, stream, reps=10) if leg_on(args, "down") else None
+        runs = {"twell_step": lambda: (L.up(), L.down(), L.bwd())}
+        if D is not None:
+            runs["dense_step"] = lambda: (D.fwd(), D.bwd())
+        energy = energy_leg(tw, local_rank, runs, inp.M)
+        if energy.get("twell_step") and energy.get("dense_step"):
+            energy["twell_over_dense_per_token"] = (energy["twell_step"]["uJ_per_token"] /
+                                                    energy["dense_step"]["uJ_per_token"])
+    if D is not None:
+        D.free()
+        del D
+        torch.cuda.empty_cache()
+
+    union = down_variants(tw, L.buf, L.Wd, L.y, L.st, flush, stream) if leg_on(args, "down") else None
+    memory = None
+    if leg_on(args, "memory"):
+        del L
+        torch.cuda.empty_cache()
+        memory = training_memory_leg(tw, inp, L1)
+    inference = inference_leg(tw, flush, stream, peaks)[0] if leg_on(args, "inference") else None
     decode = decode_leg(tw, peaks, flush, stream) if leg_on(args, "decode") else None
     hybrid = hybrid_leg(tw, flush, stream) if leg_on(args, "hybrid") else None
-    training = training_leg(tw, flush, stream) if leg_on(args, "training") else None
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.no_extras:
-        rate, S, dt, cores, done = oracle_rate(inp, args.cpu_budget)
+        rate, S, dt, cores, done, one = oracle_rate(inp, args.cpu_budget)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"first {S} of {inp.M} tokens, same weights, fwd + bwd, repeated: {done} tokens in {dt:.1f} s"}
+               "sample": f"first {S} of {inp.M} tokens, same weights, fwd + bwd, repeated: {done} tokens in {dt:.1f} s",
+               "one_core": one}
 
     if rank != 0:
         return
@@ -929,8 +1131,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "config": {"workload": WORKLOAD, "M": inp.M, "d_model": inp.d, "d_ff": inp.F, "T": inp.T, "bias": -2.33,
                    "l1": L1, "l2": "flushed between timed steps (512 MB write, then 512 MB read: clean lines)",
                    "parallelism": f"replicas x{world}", "measured_density": nnz / (inp.M * inp.F),
-                   "padding_ratio": slots / max(nnz, 1),
-                   "slots": slots},
+                   "padding_ratio": slots / max(nnz, 1), "slots": slots},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -939,10 +1140,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "fwd": {"value": world * inp.M / (ms_fwd / 1000.0), "unit": UNIT, "ms": ms_fwd},
         "stages": stages,
         "kernels": kernels,
-        "dense_tcgen05_fwd_ms": dense_ms,
+        "ceilings": {"fma": fma, "gather_TBs": gath, "hbm_GBs": peaks["hbm"], "bf16_TFLOPs": peaks["bf16"]},
+        "dense_tcgen05": dense,
+        "inference_fwd": inference,
+        "pages_context": PAGES_CONTEXT,
         "down_projection": union,
         "hybrid": hybrid,
-        "training": training,
         "energy": energy,
         "memory": memory,
         "decode": decode,
@@ -954,14 +1157,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e, dense and CPU legs (profiling runs)")
     ap.add_argument("--legs", default="all",
-                    help="comma list of the extra legs to run: e2e, dense, energy, down, decode, hybrid, training "
+                    help="comma list of the extra legs to run: e2e, dense, inference, energy, memory, down, decode, "
+                         "hybrid "
                          "(default all; --no-extras runs none)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

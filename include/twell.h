@@ -284,14 +284,42 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
 /*
  * twell_dense_ffn_fwd — the same ReLU layer computed densely with the same
  * tcgen05 GEMM (a baseline for the sparse path, not part of the method):
- *   h_dense = bf16(relu(x W_up^T + b))   [M, F] bf16 (written)
+ *   h_dense = bf16(relu(x W_up^T + b))   [M, F] bf16 (written; the dense
+ *                                        backward's mask)
  *   y       = h_dense W_down             [M, d] bf16
- *   W_downT is W_down transposed, [d, F] bf16 (the dense GEMM reads both
- *   operands K-major).
+ * Every argument has the layout of twell_ffn_fwd's; W_down [F, d] is read as
+ * the MN-major operand of the second GEMM (no transposed copy). All pointers
+ * 16-byte aligned; d % 8 == 0, F % 8 == 0. Runs on CTA pairs (TWELL_ERR_CUDA
+ * if a cluster of two cannot be launched).
  */
 twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const float* b,
-                                 const uint16_t* W_downT, int M, int d, int F,
+                                 const uint16_t* W_down, int M, int d, int F,
                                  uint16_t* h_dense, uint16_t* y, int32_t* status, void* stream);
+
+/*
+ * twell_dense_ffn_bwd — backward of the dense baseline layer, the loss and
+ * gradients of twell_ffn_bwd (L = <dy, y> + l1_coef * sum |h|) computed with
+ * dense tcgen05 GEMMs (a baseline, not part of the method):
+ *   dpre    = bf16((dy W_down^T + l1_coef) * 1[h_dense != 0])  [M, F] (workspace)
+ *   db      = sum over rows of the fp32 values before that rounding
+ *   dx      = dpre W_up          [M, d] bf16
+ *   dW_up   = dpre^T x           [F, d] fp32
+ *   dW_down = h_dense^T dy       [F, d] fp32
+ * dpre is a bf16 GEMM operand, as in a bf16 training step. The token axis is
+ * the inner dimension of the two weight-gradient GEMMs: x, dy, dpre and
+ * h_dense are read as MN-major operands, so nothing is transposed.
+ *   h_dense: the forward's [M, F] bf16 hidden matrix (twell_dense_ffn_fwd).
+ *   ws: at least twell_dense_bwd_workspace_bytes(M, d, F) bytes, 256-byte
+ *   aligned (dpre and per-128-row column sums of it).
+ * All pointers 16-byte aligned; d % 8 == 0, F % 8 == 0. Fixed summation order
+ * (no atomics). Runs on CTA pairs (TWELL_ERR_CUDA if a cluster of two cannot
+ * be launched).
+ */
+size_t twell_dense_bwd_workspace_bytes(int M, int d, int F);
+twell_status twell_dense_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16_t* W_down,
+                                 const uint16_t* h_dense, const uint16_t* dy, int M, int d, int F,
+                                 float l1_coef, uint16_t* dx, float* dW_up, float* dW_down, float* db,
+                                 void* ws, size_t ws_bytes, int32_t* status, void* stream);
 
 /*
  * twell_ffn_fwd_static_ws — twell_ffn_fwd for callers that cannot allocate
@@ -303,13 +331,21 @@ twell_status twell_dense_ffn_fwd(const uint16_t* x, const uint16_t* W_up, const 
  * the workspace is a library-owned device array of TWELL_STATIC_WS_BYTES that
  * every GPU which loads the library keeps until the process exits.
  *   - Returns TWELL_ERR_WORKSPACE, with nothing enqueued, when the problem
- *     needs more workspace than the array holds
- *     (twell_workspace_bytes(TWELL_OP_FFN_FWD or TWELL_OP_GATED_FWD, M, d, F,
- *     T, h_out->cap_slots) > TWELL_STATIC_WS_BYTES); decode shapes such as
- *     M <= 64, d_model = 4096, d_ff = 14336 fit.
+ *     needs more workspace than the array holds: gated, when
+ *     twell_workspace_bytes(TWELL_OP_GATED_FWD, M, d, F, T, h_out->cap_slots)
+ *     > TWELL_STATIC_WS_BYTES; ReLU, when even the smallest epilogue staging
+ *     (twell_fwd_workspace_bytes(M, d, F, T, h_out->cap_slots, 32)) does not
+ *     fit. A ReLU call that fits runs with the largest staging capacity (256,
+ *     64 or 32 entries per row and 256-column block) the array holds, and a
+ *     block with more active units than that reports TWELL_ERR_CAPACITY in
+ *     *status. Decode shapes such as M <= 64, d_model = 4096, d_ff = 14336
+ *     fit in both modes, and so does the ReLU layer at M = 4096, d_model =
+ *     2048, d_ff = 8192 (32-entry staging).
  *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress); make that first call before any stream
- *     capture.
+ *     device (cudaGetSymbolAddress) and keeps it for the life of the process;
+ *     make that first call before any stream capture. The kept address is
+ *     that of the device's current context: after cudaDeviceReset on a device,
+ *     do not call this entry point on it again.
  *   - All calls on a device share the one array, which keeps the last call's
  *     contents: calls whose work overlaps on the GPU (different streams, or
  *     different host threads, without ordering between them) race on it and
@@ -358,24 +394,6 @@ twell_status twell_set_kernel_timer(int site, void* ev_begin, void* ev_end);
  * pointers.
  */
 twell_status twell_wait_selftest(int which, int32_t* scratch, int32_t* status, void* stream);
-
-/*
- * twell_gather_probe — measurement aid: the memory access pattern of the
- * library's sparse kernels without their arithmetic, so that their time can be
- * set against the gather rate of the GPU they run on. One warp per (row r,
- * 256-column group g) reads, for k < nnz, the 16 bytes of W[idx[r*nnz + k]]
- * at columns 256 g + 8 lane .. +7 (eight 128-bit loads per lane in flight)
- * and writes one checksum float per task to sink.
- *   W    [F, d] bf16 row-major, device, 16-byte aligned, d a multiple of 8
- *   idx  [rows, nnz] int32, device; values are clamped into [0, F)
- *   sink [rows * ceil(d/256)] float, device, written
- * Bytes gathered per call: rows * nnz * d * 2. Asynchronous on `stream`.
- * Errors: TWELL_ERR_INVALID_ARG (null pointer, non-positive F/d/rows, negative
- * nnz, d % 8 != 0, W misaligned), TWELL_ERR_UNSUPPORTED (grid too large),
- * TWELL_ERR_CUDA (launch failed).
- */
-twell_status twell_gather_probe(const uint16_t* W, int F, int d, const int32_t* idx, int rows, int nnz, float* sink,
-                                void* stream);
 
 /* Number of kernels this library has launched in this process (host-side
  * counter, all devices). Lets a caller count the library's launches in a

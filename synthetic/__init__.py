@@ -63,11 +63,35 @@ def uniform(seed: int, stream: int, count: int, start: int = 0) -> np.ndarray:
     return ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
 
 
-def normal(seed: int, stream: int, count: int) -> np.ndarray:
-    """Standard normals by Box–Muller; element i uses uniforms 2i and 2i+1."""
-    u = uniform(seed, stream, 2 * count)
+def _normal_range(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    u = uniform(seed, stream, 2 * count, start=2 * start)
     u1, u2 = u[0::2], u[1::2]
     return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+
+
+_CHUNK = 1 << 21
+
+
+def normal(seed: int, stream: int, count: int) -> np.ndarray:
+    """Standard normals by Box–Muller; element i uses uniforms 2i and 2i+1.
+
+    Large draws are computed in chunks on a thread pool (numpy releases the
+    interpreter lock inside its array loops); every element still depends only
+    on (seed, stream, i), so the result is the same as one sequential draw."""
+    if count <= 2 * _CHUNK:
+        return _normal_range(seed, stream, 0, count)
+    import concurrent.futures as cf
+    import os
+    out = np.empty(count, dtype=np.float64)
+    starts = list(range(0, count, _CHUNK))
+
+    def one(s0: int) -> None:
+        n = min(_CHUNK, count - s0)
+        out[s0:s0 + n] = _normal_range(seed, stream, s0, n)
+
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        list(ex.map(one, starts))
+    return out
 
 
 def normal_at(seed: int, stream: int, index: np.ndarray) -> np.ndarray:
@@ -210,10 +234,23 @@ CONFIGS = {
     "decode8": dict(M=8, d=4096, F=14336, T=8, bias=-2.58, gated=True),
     "decode64": dict(M=64, d=4096, F=14336, T=64, bias=-2.58, gated=True),
     "training": dict(M=16384, d=4096, F=16384, T=128, bias=-2.33, gated=False, l1=1e-4),
+    # sparsity/skew sweep, nominal biases: Phi^-1 of the target density, the
+    # bias that gives it without skew (with the row scales the realised
+    # density is higher: about 14 / 7.4 / 5.1 %)
     "sweep90": dict(M=8192, d=4096, F=16384, T=128, bias=-1.2816, gated=False, skew=1.0),
     "sweep99": dict(M=8192, d=4096, F=16384, T=128, bias=-2.3263, gated=False, skew=1.0),
     "sweep999": dict(M=8192, d=4096, F=16384, T=128, bias=-3.0902, gated=False, skew=1.0),
+    # the same with skew-corrected biases: b solves E_s[Phi(b / s)] = 10 / 1 / 0.1 %
+    # for s ~ LogNormal(0, 1), the density of ReLU(s z + b) with z ~ N(0, 1)
+    # (x . w is ~N(0, 1) for x ~ N(0, I), w ~ N(0, I / d_model))
+    "sweep90s": dict(M=8192, d=4096, F=16384, T=128, bias=-1.8108, gated=False, skew=1.0),
+    "sweep99s": dict(M=8192, d=4096, F=16384, T=128, bias=-7.8373, gated=False, skew=1.0),
+    "sweep999s": dict(M=8192, d=4096, F=16384, T=128, bias=-20.2430, gated=False, skew=1.0),
 }
+
+# Target hidden density of each sweep workload (fraction of active units).
+SWEEP_TARGETS = {"sweep90": 0.10, "sweep99": 0.01, "sweep999": 0.001,
+                 "sweep90s": 0.10, "sweep99s": 0.01, "sweep999s": 0.001}
 
 
 def config_inputs(name: str, *, seed: int = 0, with_dy: bool = False) -> FFNInputs:

@@ -108,6 +108,26 @@ def assert_close_rms(got: np.ndarray, ref: np.ndarray, tol: float = RMS_TOL, wha
     return err, rms
 
 
+def assert_close_rms_plus(got: np.ndarray, ref: np.ndarray, bound: np.ndarray, tol: float = RMS_TOL,
+                          what: str = "", bf16_out: bool = False):
+    """assert_close_rms with a per-element allowance `bound` on top: used where
+    an operand is rounded to bf16 by design (the dense baseline's dpre), with
+    bound = that rounding's worst-case effect on the element."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    if not ref.size:
+        return 0.0, 0.0
+    if bf16_out:
+        ref_q = oracle.bf16_to_f64(oracle.round_bf16(ref.astype(np.float32)))
+        err = float(np.max(np.abs(got - ref_q) - bf16_ulp(ref_q) - bound))
+    else:
+        err = float(np.max(np.abs(got - ref) - bound))
+    assert err <= tol * rms + 1e-30, f"{what}: max|err| - bound {err:.3e} > {tol} * rms {rms:.3e}"
+    return err, rms
+
+
 def preact_tau(x_bits: np.ndarray, W_bits: np.ndarray, pre: np.ndarray) -> np.ndarray:
     """Per-entry bound tau on |fp32 pre-activation - oracle| (see module doc)."""
     d = x_bits.shape[1]

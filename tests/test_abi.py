@@ -71,11 +71,17 @@ def test_host_argument_errors_need_no_gpu(lib):
     assert rc == 1
     rc = lib.twell_check(None, None, None)
     assert rc == 1
-    rc = lib.twell_gather_probe(None, 8192, 2048, None, 4096, 82, None, None)
+    rc = lib.twell_dense_ffn_fwd(None, None, None, None, 64, 128, 512, None, None, None, None)
+    assert rc == 1
+    rc = lib.twell_dense_ffn_bwd(None, None, None, None, None, 64, 128, 512, 0.0, None, None, None, None, None, 0,
+                                 None, None)
     assert rc == 1
     fake = ctypes.c_void_p(256)  # never dereferenced: d % 8 != 0 is rejected first
-    rc = lib.twell_gather_probe(fake, 8192, 2044, fake, 4096, 82, fake, None)
+    rc = lib.twell_dense_ffn_bwd(fake, fake, fake, fake, fake, 64, 124, 512, 0.0, fake, fake, fake, fake, fake,
+                                 1 << 20, fake, None)
     assert rc == 1
+    assert lib.twell_dense_bwd_workspace_bytes(64, 124, 512) == 0
+    assert lib.twell_dense_bwd_workspace_bytes(256, 128, 512) == 256 * 512 * 2 + 2 * 512 * 4
     assert lib.twell_set_kernel_timer(11, None, None) == 1  # no such call site
     rc = lib.twell_spmm_down_tc(None, None, 128, None, None, 0, None, None)
     assert rc == 1

@@ -108,11 +108,13 @@ def test_hybrid_without_overflow_is_the_twell_forward():
     np.testing.assert_array_equal(host_bf16_bits(y), host_bf16_bits(y2))
 
 
-def test_hybrid_sweep90_full_size_sampled_rows():
-    """The skewed 90 % workload at full size (8192 x 4096 x 16384) in the
-    configuration the benchmark times (C = 1.25 % of d_ff, room for every row):
-    y and h on sampled overflow and TwELL rows against the oracle."""
-    inp = syn.config_inputs("sweep90")
+@pytest.mark.parametrize("name", ["sweep90", "sweep90s", "sweep99s", "sweep999s"])
+def test_hybrid_sweep_full_size_sampled_rows(name):
+    """The skewed sweep workloads at full size (8192 x 4096 x 16384; nominal
+    90 % and the skew-corrected 90 / 99 / 99.9 % biases) in the configuration
+    the benchmark times (C = 1.25 % of d_ff, room for every row): y and h on
+    sampled overflow and TwELL rows against the oracle."""
+    inp = syn.config_inputs(name)
     M, d, F, T = inp.M, inp.d, inp.F, inp.T
     C = round(0.0125 * F)
     buf, ov, y, st = _hybrid(inp, C, cap_rows=M, cap=M * C)
@@ -168,15 +170,17 @@ def _hybrid_bwd(inp, h_bits, C, cap_rows, l1):
     return n, bf16_f64(host_bf16_bits(dx)), dWu.cpu().numpy(), dWd.cpu().numpy(), db.cpu().numpy()
 
 
-@pytest.mark.parametrize("M,d,F,T,C,cap_extra,l1,seed", [
-    (300, 256, 1024, 32, 60, 0, 1e-3, 2),    # several pair tiles of overflow rows; skewed 10 % density
-    (90, 136, 264, 7, 12, 40, 0.0, 3),       # ragged d and F, room for more rows than overflow
-    (200, 128, 520, 16, 300, 8, 5e-2, 4),    # nothing overflows: the sparse backward alone
+@pytest.mark.parametrize("M,d,F,T,C,cap_extra,l1,seed,bias", [
+    (300, 256, 1024, 32, 60, 0, 1e-3, 2, -1.2816),   # several pair tiles of overflow rows; skewed 14 % density
+    (90, 136, 264, 7, 12, 40, 0.0, 3, -1.2816),      # ragged d and F, room for more rows than overflow
+    (200, 128, 520, 16, 300, 8, 5e-2, 4, -1.2816),   # nothing overflows: the sparse backward alone
+    (300, 256, 1024, 32, 30, 0, 1e-3, 5, -7.8373),   # skew-corrected 99 %: few dense rows, most empty
+    (600, 256, 1024, 64, 12, 0, 1e-3, 6, -20.2430),  # skew-corrected 99.9 %
 ])
-def test_hybrid_backward_matches_oracle(M, d, F, T, C, cap_extra, l1, seed):
+def test_hybrid_backward_matches_oracle(M, d, F, T, C, cap_extra, l1, seed, bias):
     # the hybrid format is another storage of the same h: the gradients are
     # the plain backward's, compared with the oracle's on the full h
-    inp = syn.ffn_inputs(M, d, F, T, -1.2816, seed=seed, with_dy=True, row_skew_sigma=1.0)
+    inp = syn.ffn_inputs(M, d, F, T, bias, seed=seed, with_dy=True, row_skew_sigma=1.0)
     fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, want_y=False)
     counts = ((fw["h"] & 0x7FFF) != 0).sum(1)
     cap_rows = int((counts > C).sum()) + cap_extra

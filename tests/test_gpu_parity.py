@@ -7,8 +7,8 @@ import torch
 
 import oracle
 import synthetic as syn
-from helpers import (assert_close_rms, assert_twell_identical, bf16_f64, compare_hidden, dev_bf16, dev_f32,
-                     host_bf16_bits, preact_tau, status_tensor, twell_to_device, twell_to_host)
+from helpers import (assert_close_rms, assert_close_rms_plus, assert_twell_identical, bf16_f64, compare_hidden,
+                     dev_bf16, dev_f32, host_bf16_bits, preact_tau, status_tensor, twell_to_device, twell_to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -313,20 +313,107 @@ def test_bwd_is_deterministic():
 
 # ------------------------------------------------------ dense baseline ------
 
-@pytest.mark.parametrize("M,d,F", [(64, 128, 512), (200, 264, 520)])
+@pytest.mark.parametrize("M,d,F", [(64, 128, 512), (200, 264, 520), (520, 1032, 776)])
 def test_dense_baseline_matches_oracle(M, d, F):
     inp = syn.ffn_inputs(M, d, F, 16, -1.0, seed=6)
     h = torch.empty(M, F, dtype=torch.int16, device="cuda")
     y = torch.empty(M, d, dtype=torch.int16, device="cuda")
-    WdT = np.ascontiguousarray(inp.W_down.T)
     st = status_tensor()
-    tw.twell_dense_ffn_fwd(dev_bf16(inp.x), dev_bf16(inp.W_up), dev_f32(inp.b), dev_bf16(WdT), h, y, st)
+    tw.twell_dense_ffn_fwd(dev_bf16(inp.x), dev_bf16(inp.W_up), dev_f32(inp.b), dev_bf16(inp.W_down), h, y, st)
     _status_ok(st)
     ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F)
     hg = host_bf16_bits(h)
     tau = preact_tau(inp.x, inp.W_up, ref["pre"])
     compare_hidden(hg, ref["h"], hg != 0, ref["active"] != 0, ref["pre"], tau)
     assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="dense y", bf16_out=True)
+
+
+def _dense_bwd(x, W_up, W_down, h, dy, l1):
+    M, d = x.shape
+    F = W_up.shape[0]
+    dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+    db = torch.empty(F, dtype=torch.float32, device="cuda")
+    ws = torch.empty(tw.twell_dense_bwd_workspace_bytes(M, d, F), dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    tw.twell_dense_ffn_bwd(dev_bf16(x), dev_bf16(W_up), dev_bf16(W_down), dev_bf16(h), dev_bf16(dy), l1, dx, dWu,
+                           dWd, db, ws, st)
+    _status_ok(st)
+    return bf16_f64(host_bf16_bits(dx)), dWu.cpu().numpy(), dWd.cpu().numpy(), db.cpu().numpy()
+
+
+# The dense baseline keeps dpre in bf16 as a GEMM operand, as a bf16 training
+# step does: each product dpre_rj * v then carries a relative error of at most
+# 2^-9 (the bf16 rounding of dpre), so dx and dW_up may differ from the fp64
+# oracle by up to 2^-9 * sum |dpre| |v| beyond the usual 2e-2 * rms (twice that
+# is allowed). dW_down (h and dy are exact bf16 inputs) and db (summed from the
+# fp32 values) take the plain bound.
+DPRE_BF16 = 2.0 ** -8
+
+
+@pytest.mark.parametrize("M,d,F,bias,l1,seed", [
+    (64, 128, 512, -2.33, 1e-4, 0),    # tiny: one CTA pair, partial tiles
+    (200, 264, 520, -1.0, 0.0, 1),     # ragged M, d, F (MN-major boxes past the edge)
+    (520, 1032, 776, -1.5, 5e-2, 2),   # several 256-wide tiles each way, large l1
+])
+def test_dense_bwd_matches_oracle(M, d, F, bias, l1, seed):
+    """The dense baseline's backward: same loss and gradients as the TwELL
+    backward, with the oracle's h as the mask (no oracle input from the GPU)."""
+    inp = syn.ffn_inputs(M, d, F, 16, bias, seed=seed, with_dy=True)
+    fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, want_y=False)
+    dx, dWu, dWd, db = _dense_bwd(inp.x, inp.W_up, inp.W_down, fw["h"], inp.dy, l1)
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, fw["h"], inp.dy))
+    dpre, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1)
+    assert_close_rms_plus(dx, dx_ref, DPRE_BF16 * (np.abs(dpre) @ np.abs(Wu)), what="dense dx", bf16_out=True)
+    assert_close_rms_plus(dWu, gu, DPRE_BF16 * (np.abs(dpre).T @ np.abs(X)), what="dense dW_up")
+    assert_close_rms(dWd, gd, what="dense dW_down")
+    assert_close_rms(db, gb, what="dense db")
+    unused = np.flatnonzero((fw["h"] != 0).sum(0) == 0)
+    assert np.all(dWu[unused] == 0) and np.all(dWd[unused] == 0) and np.all(db[unused] == 0)
+
+
+def test_dense_bwd_integer_inputs_exact():
+    """Integer-valued dy, W_down, x, W_up and h with l1 = 0 and d_model = 16:
+    |dpre| <= 16 * 4 * 4 = 256 is an integer bf16 holds exactly, and every sum
+    of the four GEMMs is an integer below 2^24, so the fp32 results are exact
+    and dx is exactly the bf16 rounding of the exact value."""
+    M, d, F = 300, 16, 264
+    inp = syn.integer_ffn_inputs(M, d, F, 16, seed=3, lo=-4, hi=4)
+    dyi = syn.integer_ffn_inputs(M, d, F, 16, seed=4, lo=-4, hi=4).x
+    h = syn.integer_ffn_inputs(M, F, F, 16, seed=5, lo=-2, hi=3).x  # [M, F] integers
+    h = np.where(oracle.bf16_to_f64(h) > 0, h, 0).astype(np.uint16)
+    dx, dWu, dWd, db = _dense_bwd(inp.x, inp.W_up, inp.W_down, h, dyi, 0.0)
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, h, dyi))
+    dpre = (DY @ Wd.T) * (H != 0)
+    assert np.abs(dpre).max() <= 256
+    dx_exact = dpre @ Wu
+    np.testing.assert_array_equal(dx, bf16_f64(oracle.round_bf16(dx_exact.astype(np.float32))))
+    np.testing.assert_array_equal(dWu, dpre.T @ X)
+    np.testing.assert_array_equal(dWd, H.T @ DY)
+    np.testing.assert_array_equal(db, dpre.sum(0))
+
+
+def test_dense_bwd_training_full_size_sampled():
+    """The dense backward at the training workload's size (M=16384, d=4096,
+    F=16384) on a 99 %-sparse h, sampled rows and columns against the oracle."""
+    M, d, F, l1 = 16384, 4096, 16384, 1e-4
+    h = syn.sparse_hidden(M, F, 0.0099, seed=31)
+    inp = syn.ffn_inputs(M, d, F, 128, -2.33, seed=31, with_dy=True)
+    dx, dWu, dWd, db = _dense_bwd(inp.x, inp.W_up, inp.W_down, h, inp.dy, l1)
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, h, inp.dy))
+    rng = np.random.default_rng(7)
+    rows = np.r_[0, M - 1, rng.integers(0, M, 10)].astype(np.int32)
+    cols = np.r_[0, F - 1, rng.integers(0, F, 10)].astype(np.int32)
+    dpre_rows, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1, rows=rows)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1, cols=cols)
+    dpre_cols = (DY @ Wd[cols].T + l1) * (H[:, cols] != 0)  # [M, len(cols)], the bound's |dpre| only
+    assert_close_rms_plus(dx[rows], dx_ref, DPRE_BF16 * (np.abs(dpre_rows) @ np.abs(Wu)), what="dense dx rows",
+                          bf16_out=True)
+    assert_close_rms_plus(dWu[cols], gu, DPRE_BF16 * (np.abs(dpre_cols).T @ np.abs(X)), what="dense dW_up cols")
+    assert_close_rms(dWd[cols], gd, what="dense dW_down cols")
+    assert_close_rms(db[cols], gb, what="dense db cols")
 
 
 # ------------------------------------------- training and skewed workloads ---
@@ -373,7 +460,7 @@ def test_bwd_training_full_size_sampled():
     assert_close_rms(db[cols], gb, what="db cols")
 
 
-@pytest.mark.parametrize("name", ["sweep90", "sweep99", "sweep999"])
+@pytest.mark.parametrize("name", ["sweep90", "sweep99", "sweep999", "sweep90s", "sweep99s", "sweep999s"])
 def test_fwd_skewed_rows(name):
     """Sweep workloads (d_model 4096, d_ff 16384, lognormal row scales on x) on
     1024 of their 8192 token rows: uneven rows stretch the tile widths."""
@@ -401,24 +488,25 @@ def test_fwd_skewed_rows(name):
     assert got.K.max() > 2 * got.nnz.mean()
 
 
-def test_gather_probe_reads_the_named_rows():
-    # the gather-ceiling probe must touch exactly W[idx[r, k], 256 g + 8 lane .. +7]:
-    # its per-task checksum (xor of every 32-bit word read, 23 low bits) is recomputed here
-    F, d, rows, nnz = 300, 520, 37, 45
-    rng = np.random.default_rng(5)
-    W = rng.integers(-32768, 32767, size=(F, d), dtype=np.int16)
-    idx = rng.integers(0, F, size=(rows, nnz), dtype=np.int32)
-    G = (d + 255) // 256
-    sink = torch.empty(rows * G, dtype=torch.float32, device="cuda")
-    tw.twell_gather_probe(torch.from_numpy(W).cuda(), torch.from_numpy(idx).cuda(), sink)
-    got = sink.cpu().numpy().view(np.uint32)
-    words = W.view(np.uint32).reshape(F, d // 2)
-    want = np.zeros(rows * G, dtype=np.uint32)
-    for r in range(rows):
-        for g in range(G):
-            c = words[idx[r], g * 128:min((g + 1) * 128, d // 2)]
-            want[r * G + g] = np.bitwise_xor.reduce(c.reshape(-1)) & 0x007fffff
-    np.testing.assert_array_equal(got, want)
+@pytest.mark.parametrize("name", ["sweep90s", "sweep99s", "sweep999s"])
+def test_bwd_skewed_rows(name):
+    """The backward on skewed rows at the sweep's skew-corrected biases (10 /
+    1 / 0.1 % density; lognormal row scales), on 512 tokens, d_model 1024,
+    d_ff 4096: some rows dense, most nearly empty, wide padded tiles."""
+    c = syn.CONFIGS[name]
+    M, d, F, T, l1 = 512, 1024, 4096, 128, 1e-4
+    inp = syn.ffn_inputs(M, d, F, T, c["bias"], seed=8, with_dy=True, row_skew_sigma=c["skew"])
+    fw = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, want_y=False)
+    ref_tw = oracle.twell_pack(fw["h"], T)
+    assert ref_tw.K.max() > 4 * max(ref_tw.nnz.mean(), 1.0)
+    dx, dWu, dWd, db = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, l1)
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, fw["h"], inp.dy))
+    _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1)
+    assert_close_rms(dx, dx_ref, what="dx", bf16_out=True)
+    assert_close_rms(dWu, gu, what="dW_up")
+    assert_close_rms(dWd, gd, what="dW_down")
+    assert_close_rms(db, gb, what="db")
 
 
 def _fwd_with_stage_cap(inp, stage_cap):

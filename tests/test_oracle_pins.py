@@ -369,3 +369,45 @@ def test_generator_is_counter_based_and_seeded():
     assert abs(a.mean()) < 0.15 and abs(a.std() - 1) < 0.1
     np.testing.assert_array_equal(syn.to_bf16_bits(a.astype(np.float32)),
                                   _torch_bf16_bits(a.astype(np.float32)))
+
+
+def test_generator_threaded_draw_equals_sequential():
+    # large draws run in chunks on a thread pool; element i must not depend on the chunking
+    n = 5 * (1 << 21) + 17
+    big = syn.normal(2, syn.STREAM_W_UP, n)
+    idx = np.array([0, 1, (1 << 21) - 1, 1 << 21, n - 1])
+    np.testing.assert_array_equal(big[idx], syn.normal_at(2, syn.STREAM_W_UP, idx))
+    np.testing.assert_array_equal(big[:1000], syn.normal(2, syn.STREAM_W_UP, 1000))
+
+
+def _skew_density(bias: float, sigma: float = 1.0) -> float:
+    """E_s[Phi(b / s)], s ~ LogNormal(0, sigma): numerical quadrature over z ~ N(0, 1)."""
+    from scipy import integrate, stats
+    f = lambda z: stats.norm.cdf(bias / math.exp(sigma * z)) * stats.norm.pdf(z)  # noqa: E731
+    return integrate.quad(f, -12, 12, limit=400, epsabs=1e-14)[0]
+
+
+@pytest.mark.parametrize("name", ["sweep90s", "sweep99s", "sweep999s"])
+def test_skew_corrected_bias_gives_target_density(name):
+    """The sweep's skew-corrected biases: (a) the closed-form expectation of the
+    hidden density under LogNormal(0, 1) row scales equals the target at the
+    stored bias; (b) the oracle's realised density on seeded skewed inputs
+    (8192 tokens, d_ff 1024, d_model 256: the same distribution of x . w) lies
+    within 5 standard deviations of the target, the deviation counting the
+    spread of the row scales as well as the per-row binomial noise."""
+    pytest.importorskip("scipy")
+    from scipy import integrate, stats
+    c, target = syn.CONFIGS[name], syn.SWEEP_TARGETS[name]
+    b = c["bias"]
+    assert abs(_skew_density(b) - target) < 1e-3 * target
+    # the nominal bias (no skew correction) gives a clearly higher density
+    nominal = syn.CONFIGS[name[:-1]]["bias"]
+    assert _skew_density(nominal) > 1.4 * target
+    M, d, F = 8192, 256, 1024
+    inp = syn.ffn_inputs(M, d, F, 128, b, seed=0, row_skew_sigma=1.0)
+    out = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, want_y=False)
+    dens = float(out["active"].mean())
+    f2 = lambda z: stats.norm.cdf(b / math.exp(z)) ** 2 * stats.norm.pdf(z)  # noqa: E731
+    e2 = integrate.quad(f2, -12, 12, limit=400, epsabs=1e-16)[0]
+    var = ((e2 - target ** 2) + (target - e2) / F) / M
+    assert abs(dens - target) < 5 * math.sqrt(var), (name, dens, target, math.sqrt(var))

@@ -48,17 +48,23 @@ def _regular(inp, cap):
     return twell_to_host(buf), bf16_f64(host_bf16_bits(y))
 
 
-def _static(inp, cap):
+def _static_call(lib, inp, buf, y, st, dev):
     """One call of twell_ffn_fwd_static_ws straight through the C ABI (ctypes)."""
+    x, Wu, Wg, b, Wd = dev
+    return lib.twell_ffn_fwd_static_ws(_vp(x), _vp(Wu), _vp(Wg), _vp(b), _vp(Wd), inp.M, inp.d, inp.F, inp.T,
+                                       buf.ref, _vp(y), _vp(st),
+                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def _static(inp, cap):
     lib = tw.load_library()
     M, d, F, T = inp.M, inp.d, inp.F, inp.T
     buf = tw.TwellBuffers(M, F, T, cap)
     y = torch.empty(M, d, dtype=torch.int16, device="cuda")
     st = status_tensor()
-    x, Wu, Wd, b = dev_bf16(inp.x), dev_bf16(inp.W_up), dev_bf16(inp.W_down), dev_f32(inp.b)
-    Wg = None if inp.W_gate is None else dev_bf16(inp.W_gate)
-    rc = lib.twell_ffn_fwd_static_ws(_vp(x), _vp(Wu), _vp(Wg), _vp(b), _vp(Wd), M, d, F, T, buf.ref, _vp(y),
-                                     _vp(st), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    dev = (dev_bf16(inp.x), dev_bf16(inp.W_up), None if inp.W_gate is None else dev_bf16(inp.W_gate),
+           dev_f32(inp.b), dev_bf16(inp.W_down))
+    rc = _static_call(lib, inp, buf, y, st, dev)
     assert rc == 0, tw.twell_status_string(rc)
     assert tw.twell_check(st) == 0
     return twell_to_host(buf), bf16_f64(host_bf16_bits(y))
@@ -77,10 +83,41 @@ def test_static_workspace_forward_matches_regular_twice(gated):
         assert_close_rms(got_y, ref_y, what="y", bf16_out=True)
 
 
+def test_static_workspace_inference_layer_with_small_staging():
+    # 4096 x 2048 x 8192 at ~99 % sparsity: only the 32-entry staging (~17 MB)
+    # fits the array; the regular call gets the full 256-entry staging
+    inp = syn.config_inputs("inference")
+    cap = inp.M * 256
+    ref_tw, ref_y = _regular(inp, cap)
+    got_tw, got_y = _static(inp, cap)
+    assert_twell_identical(got_tw, ref_tw)
+    assert_close_rms(got_y, ref_y, what="y", bf16_out=True)
+
+
+def test_static_workspace_allocates_nothing():
+    lib = tw.load_library()
+    inp = syn.ffn_inputs(64, 256, 1024, 16, -1.0, seed=13)
+    buf = tw.TwellBuffers(inp.M, inp.F, inp.T, inp.M * inp.F)
+    y = torch.empty(inp.M, inp.d, dtype=torch.int16, device="cuda")
+    st = status_tensor()
+    dev = (dev_bf16(inp.x), dev_bf16(inp.W_up), None, dev_f32(inp.b), dev_bf16(inp.W_down))
+    assert _static_call(lib, inp, buf, y, st, dev) == 0  # warm-up: first call on this device
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    launches0 = tw.twell_kernel_launches()
+    for _ in range(3):
+        assert _static_call(lib, inp, buf, y, st, dev) == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert tw.twell_check(st) == 0
+    assert tw.twell_kernel_launches() > launches0, "the forward's kernels did not run"
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+
+
 def test_static_workspace_rejects_too_large_problem():
     lib = tw.load_library()
-    M, d, F, T = 4096, 2048, 8192, 128  # needs ~134 MB of staging, more than the array
-    assert tw.twell_workspace_bytes(tw.OP_FFN_FWD, M, d, F, T, M * F) > tw.STATIC_WS_BYTES
+    M, d, F, T = 16384, 4096, 16384, 128  # even the 32-entry staging needs ~134 MB
+    assert tw.twell_fwd_workspace_bytes(M, d, F, T, M * F, 32) > tw.STATIC_WS_BYTES
     buf = tw_binding._TwellBuf(M, F, T, (M + T - 1) // T, M * F, None, None, None, None, None)
     rc = lib.twell_ffn_fwd_static_ws(None, None, None, None, None, M, d, F, T, ctypes.byref(buf), None, None, None)
     assert rc == 3  # TWELL_ERR_WORKSPACE, nothing enqueued
