@@ -401,21 +401,23 @@ def fma_peak(stream, sm_count: int):
 
 
 def gather_ceiling(W, nnz_per_row: int, reps: int = 6):
-    """Measured rate (TB/s) at which 512-byte stretches of random rows of W
-    (L2-resident) reach the SMs: four forms (128-bit loads with 4 or 8 in flight
-    per lane; bulk copies into shared memory with 3 or 6 batches in flight per
-    warp), best of `reps` each after warm-up."""
+    """Measured rate (TB/s) at which stretches of random rows of W (L2-resident)
+    reach the SMs: 128-bit loads with 4 or 8 in flight per lane in row order,
+    bulk copies into shared memory with 3 or 6 batches in flight per warp, and
+    128-bit loads in the down-projection's column-group-major order (two
+    256-column chunks per lane); best of `reps` each after warm-up. The
+    ceiling is the fastest form."""
     lib = load_probes()
     F, d = W.shape
     rows = 4096
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
     idx = torch.randint(0, F, (rows, nnz_per_row), dtype=torch.int32, device="cuda", generator=g)
-    sink = torch.empty(rows * ((d + 255) // 256), dtype=torch.float32, device="cuda")
+    sink = torch.empty(rows * ((d + 255) // 256), dtype=torch.float32, device="cuda")  # >= rows * ceil(d/512)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
     out = {}
-    for mode, name in ((0, "ldg4"), (1, "ldg8"), (2, "bulk3"), (3, "bulk6")):
+    for mode, name in ((0, "ldg4"), (1, "ldg8"), (2, "bulk3"), (3, "bulk6"), (4, "ldg_cols")):
         def call():
             rc = lib.probe_gather(mode, ctypes.c_void_p(W.data_ptr()), F, d, ctypes.c_void_p(idx.data_ptr()), rows,
                                   nnz_per_row, ctypes.c_void_p(sink.data_ptr()), ctypes.c_void_p(st.data_ptr()),
@@ -801,7 +803,7 @@ def hybrid_leg(tw, flush, stream, reps: int = 5):
         slots, nnz = buf.slots(), int(buf.nnz.sum().item())
         del ws
         down = down_variants(tw, buf, Wd, y, st, flush, stream)
-        wsb = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, max(slots, 1)), dtype=torch.uint8,
+        wsb = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, M * F), dtype=torch.uint8,
                           device="cuda")
         ms_tw_b = timed(lambda: tw.twell_ffn_bwd(x, Wu, Wd, buf, dy, l1, dx, dWu, dWd, db, wsb, st), n=2)
         del buf, wsb

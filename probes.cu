@@ -6,9 +6,10 @@
 // ceilings are therefore neither HBM bandwidth nor the tensor-core peak but
 //   - the FP32 FMA rate of the SMs (probe_fma), and
 //   - how fast row stretches named by random indices reach the SMs
-//     (probe_gather_ldg: 128-bit loads into registers, the kernels' own
-//     pattern; probe_gather_bulk: asynchronous bulk copies into shared memory,
-//     which keep more bytes in flight per SM than registers allow).
+//     (128-bit loads into registers in the kernels' own orders; and, for
+//     comparison, asynchronous bulk copies into shared memory, which keep
+//     more bytes in flight per SM than registers allow but were measured
+//     slower).
 // bench.py builds this file into _build/libprobes.so and reports each kernel
 // against the measured figures. Every wait is bounded; a probe that gives up
 // reports it in its status word.
@@ -101,6 +102,48 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_ldg(const uint16_t* __re
             const uint4 v =
                 col_ok ? __ldg(reinterpret_cast<const uint4*>(W + (size_t)j * d + c0)) : make_uint4(0, 0, 0, 0);
             acc ^= v.x ^ v.y ^ v.z ^ v.w;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) sink[task] = __uint_as_float(acc & 0x007fffffu);
+}
+
+// The down-projection's own order: warp task (column group g of 512 columns,
+// row r), task = g * rows + r, so the grid walks W one 512-column slice at a
+// time; the lane reads 16 bytes in each of its two 256-column chunks, four
+// entries (eight 128-bit loads) in flight.
+__global__ void __launch_bounds__(kWarps * 32) k_gather_cols(const uint16_t* __restrict__ W, int F, int d,
+                                                             const int32_t* __restrict__ idx, int rows, int nnz,
+                                                             float* __restrict__ sink)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = (d + 511) >> 9;
+    const long long task = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (task >= (long long)rows * G) return;
+    const int g = (int)(task / rows), r = (int)(task % rows);
+    const int c0 = g * 512 + lane * 8, c1 = c0 + 256;
+    const bool ok0 = c0 < d, ok1 = c1 < d;
+    const int32_t* ir = idx + (size_t)r * nnz;
+    uint32_t acc = 0;
+    for (int k0 = 0; k0 < nnz; k0 += 32) {
+        const int m = min(32, nnz - k0);
+        int jl = 0;
+        if (lane < m) jl = min(max(ir[k0 + lane], 0), F - 1);
+        for (int u = 0; u < m; u += 4) {
+            uint4 v[4][2];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = __shfl_sync(0xffffffffu, jl, u + q < m ? u + q : u);
+                const bool live = u + q < m;
+                v[q][0] = (live && ok0) ? __ldg(reinterpret_cast<const uint4*>(W + (size_t)j * d + c0))
+                                        : make_uint4(0, 0, 0, 0);
+                v[q][1] = (live && ok1) ? __ldg(reinterpret_cast<const uint4*>(W + (size_t)j * d + c1))
+                                        : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                acc ^= v[q][0].x ^ v[q][0].y ^ v[q][0].z ^ v[q][0].w ^ v[q][1].x ^ v[q][1].y ^ v[q][1].z ^ v[q][1].w;
         }
     }
 #pragma unroll
@@ -235,8 +278,10 @@ int probe_fma(int mode, int blocks, int iters, float* sink, void* stream)
 // int32 (clamped into [0, F)), sink [rows * ceil(d/256)] float.
 // mode 0: 128-bit loads, 4 in flight per lane; mode 1: 8 in flight; modes 2
 // and 3: bulk copies into shared memory, 3 or 6 batches of 8 rows in flight
-// per warp (d % 256 == 0). status: int32 device word, set to 1 if a bounded
-// wait gave up.
+// per warp (d % 256 == 0); mode 4: 128-bit loads in the down-projection's
+// column-group-major order, 512 columns per task (sink then holds
+// rows * ceil(d/512) floats, task g * rows + r). status: int32 device word,
+// set to 1 if a bounded wait gave up.
 int probe_gather(int mode, const uint16_t* W, int F, int d, const int32_t* idx, int rows, int nnz, float* sink,
                  int32_t* status, void* stream)
 {
@@ -251,6 +296,11 @@ int probe_gather(int mode, const uint16_t* W, int F, int d, const int32_t* idx, 
             k_gather_ldg<4><<<(unsigned)blocks, kWarps * 32, 0, s>>>(W, F, d, idx, rows, nnz, sink);
         else
             k_gather_ldg<8><<<(unsigned)blocks, kWarps * 32, 0, s>>>(W, F, d, idx, rows, nnz, sink);
+    } else if (mode == 4) {
+        const long long t4 = (long long)rows * ((d + 511) / 512);
+        const long long blocks = (t4 + kWarps - 1) / kWarps;
+        if (blocks > 0x7fffffffLL) return 1;
+        k_gather_cols<<<(unsigned)blocks, kWarps * 32, 0, s>>>(W, F, d, idx, rows, nnz, sink);
     } else if (mode == 2 || mode == 3) {
         if (d % 256 != 0) return 1;
         const long long blocks = (tasks + kBulkWarps - 1) / kBulkWarps;

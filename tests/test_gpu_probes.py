@@ -13,15 +13,16 @@ import torch
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_gather_probe_reads_the_named_rows(mode):
     import bench
     lib = bench.load_probes()
-    F, d, rows, nnz = 300, 512 if mode >= 2 else 520, 37, 45
+    F, d, rows, nnz = 300, 512 if mode in (2, 3) else 520, 37, 45
     rng = np.random.default_rng(5 + mode)
     W = rng.integers(-32768, 32767, size=(F, d), dtype=np.int16)
     idx = rng.integers(0, F, size=(rows, nnz), dtype=np.int32)
-    G = (d + 255) // 256
+    GW = 512 if mode == 4 else 256  # columns per task
+    G = (d + GW - 1) // GW
     Wd, idxd = torch.from_numpy(W).cuda(), torch.from_numpy(idx).cuda()
     sink = torch.empty(rows * G, dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -36,8 +37,9 @@ def test_gather_probe_reads_the_named_rows(mode):
     want = np.zeros(rows * G, dtype=np.uint32)
     for r in range(rows):
         for g in range(G):
-            c = words[idx[r], g * 128:min((g + 1) * 128, d // 2)]
-            want[r * G + g] = np.bitwise_xor.reduce(c.reshape(-1)) & 0x007fffff
+            c = words[idx[r], g * GW // 2:min((g + 1) * GW // 2, d // 2)]
+            task = g * rows + r if mode == 4 else r * G + g
+            want[task] = np.bitwise_xor.reduce(c.reshape(-1)) & 0x007fffff
     np.testing.assert_array_equal(got, want)
 
 
