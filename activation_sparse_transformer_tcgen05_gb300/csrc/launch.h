@@ -130,6 +130,8 @@ struct GemmArgs {
     int32_t* nnz;          // [rows], zeroed by the caller before the launch; null: not counted
     int32_t* zero_word;    // if set, written 0 by the kernel (a counter the next kernel starts from)
     const int32_t* rowsA_dev;  // if set, rows of A actually used: min(*rowsA_dev, rowsA), read on the device
+    const int32_t* K_dev;      // if set, depth actually used: *K_dev rounded up to 64, at most K, read on the
+                               //   device (both operands must be zero between *K_dev and that rounding)
     const int32_t* row_map;    // DENSE only: if set, output row of A's row i is row_map[i]
     const void* pf0;           // GATE_SWAP: rows of pf0 and pf1 (pf_row_bytes each) of the
     const void* pf1;           //   active units are prefetched into L2 (pf_row_bytes 0: off)

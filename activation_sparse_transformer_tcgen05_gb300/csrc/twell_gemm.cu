@@ -60,6 +60,17 @@ struct Layout {
     static_assert(SUB_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
 };
 
+// Depth of the contraction: a.K, or with a.K_dev the count an earlier kernel
+// wrote there, rounded up to the 64-deep k-block (the operands are zero past
+// it) and at most a.K.
+__device__ __forceinline__ int gemm_k(const GemmArgs& a)
+{
+    if (!a.K_dev) return a.K;
+    const int k = *a.K_dev;
+    const int kr = k <= 0 ? 0 : ((k + BK - 1) / BK) * BK;
+    return kr < a.K ? kr : a.K;
+}
+
 __device__ __forceinline__ void fail(int32_t* status, volatile int* abort_flag)
 {
     set_error(status, TWELL_ERR_TIMEOUT);
@@ -268,8 +279,8 @@ __global__ void __launch_bounds__(192, 1)
 
     const int num_m = (rowsA + BM - 1) / BM;
     const int num_n = (a.rowsB + BN - 1) / BN;
-    const int num_kb = (a.K + BK - 1) / BK;
-    const int num_tiles = num_m * num_n;
+    const int num_kb = (gemm_k(a) + BK - 1) / BK;
+    const int num_tiles = num_kb > 0 ? num_m * num_n : 0;  // no k-block: nothing to add or store
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
@@ -607,8 +618,8 @@ __global__ void __launch_bounds__(192, 1)
 
     const int num_m = (rowsA + PAIR_M - 1) / PAIR_M;
     const int num_n = (a.rowsB + PAIR_N - 1) / PAIR_N;
-    const int num_kb = (a.K + BK - 1) / BK;
-    const int num_tiles = num_m * num_n;
+    const int num_kb = (gemm_k(a) + BK - 1) / BK;  // same in both CTAs
+    const int num_tiles = num_kb > 0 ? num_m * num_n : 0;  // no k-block: nothing to add or store
     const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
 
     if (warp == 0) {

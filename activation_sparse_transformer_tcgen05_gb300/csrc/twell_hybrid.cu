@@ -27,6 +27,10 @@ __device__ __forceinline__ int live_rows(const int32_t* n_rows, int cap_rows)
     return n < 0 ? 0 : (n < cap_rows ? n : cap_rows);
 }
 
+// Rows of the token axis the GEMMs read: the live rows rounded up to the GEMM's
+// 64-deep k-block (the rows between are zeros). Kernels skip every row past it.
+__device__ __forceinline__ int used_rows(int n) { return (n + 63) / 64 * 64; }
+
 // dst[i, :] = src[rows[i], :] for i < n, zeros for n <= i < cap (bf16 rows of d).
 __global__ void k_gather_rows(const uint16_t* __restrict__ src, int d, const int32_t* __restrict__ rows,
                               const int32_t* __restrict__ n_rows, int cap_rows, int cap,
@@ -35,6 +39,7 @@ __global__ void k_gather_rows(const uint16_t* __restrict__ src, int d, const int
     const int i = blockIdx.x;
     if (i >= cap) return;
     const int n = live_rows(n_rows, cap_rows);
+    if (i >= used_rows(n)) return;
     uint4* out = reinterpret_cast<uint4*>(dst + (size_t)i * d);
     if (i < n) {
         const uint4* in = reinterpret_cast<const uint4*>(src + (size_t)rows[i] * d);
@@ -50,7 +55,9 @@ __global__ void k_split_rows(const float* __restrict__ src, int cols, const int3
 {
     const int i = blockIdx.x;
     if (i >= cap) return;
-    const bool live = i < live_rows(n_rows, cap_rows);
+    const int n = live_rows(n_rows, cap_rows);
+    if (i >= used_rows(n)) return;
+    const bool live = i < n;
     for (int c = threadIdx.x; c < cols; c += blockDim.x) {
         const size_t k = (size_t)i * cols + c;
         const float v = live ? src[k] : 0.f;
@@ -82,6 +89,7 @@ __global__ void k_transpose(const uint16_t* __restrict__ src, int cols, const in
     __shared__ uint16_t t[32][33];
     const int n = live_rows(n_rows, cap_rows);
     const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    if (r0 >= used_rows(n)) return;  // uniform over the block
     const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
     for (int k = ty; k < 32; k += 8) {
         const int r = r0 + k, c = c0 + tx;
@@ -149,11 +157,12 @@ size_t carve_hybrid_bwd(void* ws, int M, int d, int F, int T, int64_t cap_slots,
 
 cudaError_t dense_gemm_f32(const uint16_t* A, const uint16_t* B, int rowsA, const int32_t* rowsA_dev, int rowsB,
                            int K, float* out, int ldo, int accumulate, const uint16_t* mask, int ldm, float add,
-                           int32_t* status, int sms, cudaStream_t s)
+                           int32_t* status, int sms, cudaStream_t s, const int32_t* K_dev = nullptr)
 {
     GemmArgs g{};
     g.rowsA = rowsA;
     g.rowsA_dev = rowsA_dev;
+    g.K_dev = K_dev;
     g.rowsB = rowsB;
     g.K = K;
     g.out_f32 = out;
@@ -251,9 +260,12 @@ extern "C" twell_status twell_hybrid_ffn_bwd(const uint16_t* x, const uint16_t* 
         e = cudaGetLastError();
     }
     // dW_up += (hi + lo)^T x_R, dW_down += h_R^T dy_R
-    if (e == cudaSuccess) e = dense_gemm_f32(w.hiT, w.xRT, F, nullptr, d, cap, dW_up, d, 1, nullptr, 0, 0.f, status, sms, s);
-    if (e == cudaSuccess) e = dense_gemm_f32(w.loT, w.xRT, F, nullptr, d, cap, dW_up, d, 1, nullptr, 0, 0.f, status, sms, s);
+    // (the token axis is their depth: only the live rows, read from the device count)
     if (e == cudaSuccess)
-        e = dense_gemm_f32(w.hT, w.dyRT, F, nullptr, d, cap, dW_down, d, 1, nullptr, 0, 0.f, status, sms, s);
+        e = dense_gemm_f32(w.hiT, w.xRT, F, nullptr, d, cap, dW_up, d, 1, nullptr, 0, 0.f, status, sms, s, n);
+    if (e == cudaSuccess)
+        e = dense_gemm_f32(w.loT, w.xRT, F, nullptr, d, cap, dW_up, d, 1, nullptr, 0, 0.f, status, sms, s, n);
+    if (e == cudaSuccess)
+        e = dense_gemm_f32(w.hT, w.dyRT, F, nullptr, d, cap, dW_down, d, 1, nullptr, 0, 0.f, status, sms, s, n);
     return e == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
