@@ -27,6 +27,18 @@ import oracle
 
 RMS_TOL = 2e-2
 
+# Every floating-point comparison's margins, for the summary the test session
+# prints at its end (tests/conftest.py): (test, output, plain max|err| / rms,
+# max|err| beyond the allowance / rms, tolerance).
+MARGINS: list[tuple[str, str, float, float, float]] = []
+
+
+def _record(what: str, plain: float, beyond: float, rms: float, tol: float):
+    import os
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    if rms > 0:
+        MARGINS.append((test, what, plain / rms, beyond / rms, tol))
+
 
 def dev_bf16(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).cuda()
@@ -98,12 +110,14 @@ def assert_close_rms(got: np.ndarray, ref: np.ndarray, tol: float = RMS_TOL, wha
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     if not ref.size:
         return 0.0, 0.0
+    plain = float(np.max(np.abs(got - ref)))
     if bf16_out:
         ref_q = oracle.bf16_to_f64(oracle.round_bf16(ref.astype(np.float32)))
         excess = np.abs(got - ref_q) - bf16_ulp(ref_q)
         err = float(np.max(excess))
     else:
-        err = float(np.max(np.abs(got - ref)))
+        err = plain
+    _record(what, plain, err, rms, tol)
     assert err <= tol * rms + 1e-30, f"{what}: max|err| {err:.3e} > {tol} * rms {rms:.3e}"
     return err, rms
 
@@ -119,11 +133,13 @@ def assert_close_rms_plus(got: np.ndarray, ref: np.ndarray, bound: np.ndarray, t
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     if not ref.size:
         return 0.0, 0.0
+    plain = float(np.max(np.abs(got - ref)))
     if bf16_out:
         ref_q = oracle.bf16_to_f64(oracle.round_bf16(ref.astype(np.float32)))
         err = float(np.max(np.abs(got - ref_q) - bf16_ulp(ref_q) - bound))
     else:
         err = float(np.max(np.abs(got - ref) - bound))
+    _record(what, plain, err, rms, tol)
     assert err <= tol * rms + 1e-30, f"{what}: max|err| - bound {err:.3e} > {tol} * rms {rms:.3e}"
     return err, rms
 
