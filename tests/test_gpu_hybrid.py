@@ -203,3 +203,32 @@ def test_hybrid_backward_is_deterministic():
     assert a[0] > 0
     for u, v in zip(a[1:], b[1:]):
         np.testing.assert_array_equal(u, v)
+
+
+@pytest.mark.parametrize("density", [0.0103, 0.0012])
+def test_hybrid_backward_full_size_sampled(density):
+    """The hybrid backward at the sweep workloads' full size (8192 x 4096 x
+    16384) in the configuration the benchmark times (C = 1.25 % of d_ff, room
+    for every row), on a synthetic h whose row densities are 1.03 % or 0.12 %
+    scaled by LogNormal(0, 1) (3471 and 89 overflow rows): dx on sampled rows
+    (overflow and TwELL rows) and dW_up, dW_down, db on sampled columns against
+    the oracle on the full h."""
+    M, d, F, T, l1 = 8192, 4096, 16384, 128, 1e-4
+    C = round(0.0125 * F)
+    h = syn.sparse_hidden(M, F, density, seed=41, row_skew_sigma=1.0)
+    inp = syn.ffn_inputs(M, d, F, T, -2.33, seed=41, with_dy=True)
+    n, dx, dWu, dWd, db = _hybrid_bwd(inp, h, C, M, l1)
+    counts = ((h & 0x7FFF) != 0).sum(1)
+    rows_ov = np.flatnonzero(counts > C)
+    assert n == len(rows_ov) and 0 < n < M
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, h, inp.dy))
+    rng = np.random.default_rng(9)
+    in_ell = np.setdiff1d(np.arange(M), rows_ov)
+    rows = np.r_[rng.choice(rows_ov, min(4, n), replace=False), rng.choice(in_ell, 6, replace=False)].astype(np.int32)
+    cols = np.r_[0, F - 1, rng.integers(0, F, 10)].astype(np.int32)
+    _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1, rows=rows)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1, cols=cols)
+    assert_close_rms(dx[rows], dx_ref, what="dx rows", bf16_out=True)
+    assert_close_rms(dWu[cols], gu, what="dW_up cols")
+    assert_close_rms(dWd[cols], gd, what="dW_down cols")
+    assert_close_rms(db[cols], gb, what="db cols")

@@ -328,6 +328,25 @@ def test_dense_baseline_matches_oracle(M, d, F):
     assert_close_rms(bf16_f64(host_bf16_bits(y)), ref["y"], what="dense y", bf16_out=True)
 
 
+def test_dense_fwd_training_full_size_sampled():
+    """The dense baseline's forward at the training workload's size (16384 x
+    4096 x 16384, the shape the benchmark times it on): h and y on sampled
+    rows against the oracle."""
+    inp = syn.config_inputs("training")
+    M, d, F = inp.M, inp.d, inp.F
+    h = torch.empty(M, F, dtype=torch.int16, device="cuda")
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    st = status_tensor()
+    tw.twell_dense_ffn_fwd(dev_bf16(inp.x), dev_bf16(inp.W_up), dev_f32(inp.b), dev_bf16(inp.W_down), h, y, st)
+    _status_ok(st)
+    rows = np.r_[0, 255, 256, M - 1, np.random.default_rng(4).integers(0, M, 8)].astype(np.int32)
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F, rows=rows)
+    hg = host_bf16_bits(h)[rows]
+    tau = preact_tau(inp.x[rows], inp.W_up, ref["pre"])
+    compare_hidden(hg, ref["h"], hg != 0, ref["active"] != 0, ref["pre"], tau)
+    assert_close_rms(bf16_f64(host_bf16_bits(y))[rows], ref["y"], what="dense y rows", bf16_out=True)
+
+
 def _dense_bwd(x, W_up, W_down, h, dy, l1):
     M, d = x.shape
     F = W_up.shape[0]
