@@ -912,7 +912,32 @@ def training_memory_leg(tw, inp, l1: float):
     return out
 
 
-EXTRA_LEGS = ("e2e", "dense", "inference", "energy", "memory", "down", "decode", "hybrid")
+EXTRA_LEGS = ("e2e", "dense", "crossover", "inference", "energy", "memory", "down", "decode", "hybrid")
+
+# Biases of the training workload's shape at higher sparsity (no row skew):
+# Phi^-1 of the target density.
+CROSSOVER_BIASES = {"99.0": -2.3263, "99.5": -2.5758, "99.9": -3.0902}
+
+
+def crossover_leg(tw, L: "Layer", flush, stream, dense_step_ms, reps: int = 5):
+    """The training step on the training workload's inputs at 99 / 99.5 /
+    99.9 % nominal sparsity (only the bias changes), against the dense step
+    (whose work does not depend on the bias): where the sparse path overtakes
+    the dense layer on this GPU."""
+    out = {}
+    b0 = L.b
+    try:
+        for name, bias in CROSSOVER_BIASES.items():
+            L.b = torch.full_like(b0, bias)
+            ms = timed_ms(lambda: (L.up(), L.down(), L.bwd()), flush, stream, L.st, tw, n=reps)
+            nnz = int(L.buf.nnz.sum().item())
+            out[name] = {"bias": bias, "density": nnz / (L.inp.M * L.inp.F), "step_ms": ms,
+                         "tokens_per_s": L.inp.M / (ms / 1000.0)}
+            if dense_step_ms:
+                out[name]["sparse_vs_dense"] = dense_step_ms / ms
+    finally:
+        L.b = b0
+    return out
 
 
 def dominant_site(site_us: dict) -> int:
@@ -1101,6 +1126,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                  "sparse_step_vs_dense_step": (d_f + d_b) / ms_step,
                  "sparse_fwd_vs_dense_fwd": d_f / ms_fwd}
 
+    crossover = None
+    if leg_on(args, "crossover"):
+        crossover = crossover_leg(tw, L, flush, stream, dense["step_ms"] if dense else None)
+
     energy = None
     if leg_on(args, "energy"):
         runs = {"twell_step": lambda: (L.up(), L.down(), L.bwd())}
@@ -1152,6 +1181,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "kernels": kernels,
         "ceilings": {"fma": fma, "gather_TBs": gath, "hbm_GBs": peaks["hbm"], "bf16_TFLOPs": peaks["bf16"]},
         "dense_tcgen05": dense,
+        "sparsity_crossover": crossover,
         "inference_fwd": inference,
         "pages_context": PAGES_CONTEXT,
         "down_projection": union,
@@ -1174,8 +1204,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e, dense and CPU legs (profiling runs)")
     ap.add_argument("--legs", default="all",
-                    help="comma list of the extra legs to run: e2e, dense, inference, energy, memory, down, decode, "
-                         "hybrid "
+                    help="comma list of the extra legs to run: e2e, dense, crossover, inference, energy, memory, down, "
+                         "decode, hybrid "
                          "(default all; --no-extras runs none)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
