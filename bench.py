@@ -527,7 +527,7 @@ NCU_TRAFFIC = {
     # training workload, profiles/ncu_fwd_bwd_training_M16384.md; a call site's
     # figure is the sum over its launches (site 3: the slices and the combine;
     # site 6: the dW_down and the dW_up gathers)
-    ("training", 1): ("twell_gemm.cu", "d4eef5ff27b3ecb1837639cbf81a043fe4fea5cddca0845db075d8adacd558d4", 1542.3e6),
+    ("training", 1): ("twell_gemm.cu", "805eb0973a54da0d6f6cb4aa8684ad01ad0b8e508dbcc0da74b9a7c9dd3f241c", 1390.0e6),
     ("training", 2): ("twell_sparse.cu", "13c3ed8fa111f102332285262d735a587adaa3452034bc8262e8e67d52cd3eee", 304.1e6),
     ("training", 3): ("twell_sparse.cu", "13c3ed8fa111f102332285262d735a587adaa3452034bc8262e8e67d52cd3eee", 411.7e6),
     ("training", 4): ("twell_sparse.cu", "13c3ed8fa111f102332285262d735a587adaa3452034bc8262e8e67d52cd3eee", 345.4e6),
