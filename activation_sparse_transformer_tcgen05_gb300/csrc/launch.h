@@ -50,6 +50,11 @@ cudaError_t launch_fill_dense(const uint16_t* h, int ldh, const TwellView& tw, i
 // ov_pos (hybrid format, else null): rows with ov_pos[r] >= 0 are left empty.
 cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN, int stride,
                                     const TwellView& tw, const int32_t* ov_pos, int32_t* status, cudaStream_t s);
+// Layout and fill of a ReLU TwELL in one launch (tile widths and offsets
+// recomputed by every block), for n_tiles <= the fused kernel's limit.
+bool fused_fill_ok(int n_tiles);
+cudaError_t launch_layout_fill_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN, int stride,
+                                    const TwellView& tw, int sm_count, int32_t* status, cudaStream_t s);
 // Hybrid format: overflow rows (nnz > C) in ascending order, nnz of those rows
 // set to 0 (run before launch_tile_layout), then their dense hidden rows.
 cudaError_t launch_overflow_rows(const TwellView& tw, int C, int cap_rows, int32_t* ov_pos, int32_t* ov_rows,

@@ -365,6 +365,9 @@ twell_status up_pack_impl(const uint16_t* x, const uint16_t* W_up, const uint16_
         if (small_fill_ok(M, ga.NB)) {
             if (e == cudaSuccess)
                 e = launch_layout_fill_small_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, stage_cap, tw, status, s);
+        } else if (fused_fill_ok(tw.n_tiles)) {
+            if (e == cudaSuccess)
+                e = launch_layout_fill_relu(w.stage, w.stage_cnt, ga.NB, kReluBN, stage_cap, tw, sms, status, s);
         } else {
             if (e == cudaSuccess) e = launch_tile_layout(tw, status, s);
             if (e == cudaSuccess)

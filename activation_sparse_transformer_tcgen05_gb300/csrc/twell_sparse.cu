@@ -283,6 +283,92 @@ __global__ void k_fill_staged_relu(const uint32_t* __restrict__ stage, const int
     }
 }
 
+// Layout and fill of the ReLU TwELL in one launch (n_tiles <= kFusedFillMaxTiles):
+// every block computes the tile widths K[t] (max nnz over the tile's rows,
+// read from L2) and their compact offsets in shared memory, then fills the
+// slots of its own rows_per_block rows as k_fill_staged_relu does (a warp per
+// row). Block 0 writes K[] and off[] and reports a capacity overflow; every
+// block sees the same total and skips the fill then. This replaces the
+// single-block k_tile_layout and its dependent launch.
+constexpr int kFusedFillMaxTiles = 2048;
+
+__global__ void __launch_bounds__(1024) k_layout_fill_relu(const uint32_t* __restrict__ stage,
+                                                           const int32_t* __restrict__ stage_cnt, int NB, int BN,
+                                                           int stride, TwellView tw, int rows_per_block,
+                                                           int32_t* status)
+{
+    __shared__ int s_K[kFusedFillMaxTiles];
+    __shared__ long long s_off[kFusedFillMaxTiles + 1];
+    __shared__ long long s_warp[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (has_error(status)) return;
+    const int nt = tw.n_tiles;
+    for (int t = warp; t < nt; t += 32) {
+        const int r0 = t * tw.T, rows = min(tw.T, tw.M - r0);
+        int mx = 0;
+        for (int i = lane; i < rows; i += 32) mx = max(mx, tw.nnz[r0 + i]);
+        mx = warp_max_i(mx);
+        if (lane == 0) s_K[t] = mx;
+    }
+    __syncthreads();
+    // exclusive prefix of rows(t) * K[t]: thread i sums tiles 2i, 2i + 1
+    long long v0 = 0, v1 = 0;
+    const int t0 = 2 * tid;
+    if (t0 < nt) v0 = (long long)min(tw.T, tw.M - t0 * tw.T) * s_K[t0];
+    if (t0 + 1 < nt) v1 = (long long)min(tw.T, tw.M - (t0 + 1) * tw.T) * s_K[t0 + 1];
+    long long incl = v0 + v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    long long before = 0;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    const long long excl = before + incl - (v0 + v1);
+    if (t0 < nt) s_off[t0] = excl;
+    if (t0 + 1 < nt) s_off[t0 + 1] = excl + v0;
+    if (tid == 0) {
+        long long total = 0;
+        for (int w = 0; w < 32; ++w) total += s_warp[w];
+        s_off[nt] = total;
+    }
+    __syncthreads();
+    const bool over = s_off[nt] > tw.cap;
+    if (blockIdx.x == 0) {
+        for (int t = tid; t <= nt; t += blockDim.x) {
+            if (t < nt) tw.K[t] = s_K[t];
+            tw.off[t] = s_off[t];
+        }
+        if (tid == 0 && over) set_error(status, TWELL_ERR_CAPACITY);
+    }
+    if (over) return;  // uniform: every block computed the same layout
+    const int r_begin = blockIdx.x * rows_per_block, r_end = min(tw.M, r_begin + rows_per_block);
+    for (int r = r_begin + warp; r < r_end; r += 32) {
+        const int t = r / tw.T, Kt = s_K[t];
+        const int64_t base = s_off[t] + (int64_t)(r - t * tw.T) * Kt;
+        int pos = 0;
+        for (int nb0 = 0; nb0 < NB; nb0 += 32) {
+            const int nb = nb0 + lane;
+            const int c = nb < NB ? stage_cnt[(size_t)r * NB + nb] : 0;
+            const int ic = warp_incl_scan(c, lane);
+            const int64_t p = base + pos + (ic - c);
+            const uint32_t* src = stage + ((size_t)r * NB + nb) * stride;
+            for (int e = 0; e < c; ++e) {
+                const uint32_t w = src[e];
+                tw.idx[p + e] = nb * BN + (int)(w & 0xffffu);
+                tw.val[p + e] = (uint16_t)(w >> 16);
+            }
+            pos += __shfl_sync(0xffffffffu, ic, 31);
+        }
+        for (int k = pos + lane; k < Kt; k += 32) {
+            tw.idx[base + k] = -1;
+            tw.val[base + k] = 0;
+        }
+    }
+}
+
 // Same for the gate staging: entries (global column, fp32 gate value). The
 // values go to gval[slot]; val[] is written later by the gated-up kernel.
 __global__ void k_fill_staged_gate(const uint2* __restrict__ stage, const int32_t* __restrict__ stage_cnt, int NB,
@@ -932,12 +1018,16 @@ struct GatherArgs {
 // 16384 rows) and that slice stays in L2, whatever the size of W. Lane l holds
 // columns 256 CH g + 256 c + 8 l .. +7 of chunk c; entries come 4 at a time
 // (4 CH 128-bit loads in flight per lane).
+// Blocks of 4 warps: measured against 8 at the training size, the gathers
+// finish 1-3 % sooner (a finer grid balances the last wave better).
+constexpr int kGatherWarps = 4;
+
 template <int CH, int SRC>
-__global__ void __launch_bounds__(kWarps * 32) k_gather(GatherArgs ga, const int32_t* status)
+__global__ void __launch_bounds__(kGatherWarps * 32) k_gather(GatherArgs ga, const int32_t* status)
 {
     constexpr int GW = 256 * CH;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t task = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t task = (int64_t)blockIdx.x * kGatherWarps + warp;
     const TwellView& tw = ga.tw;
     if (has_error(status) || over_capacity(tw)) return;  // uniform across the block
     const int ntasks = SRC == SRC_TWELL ? tw.M : tw.F;
@@ -1369,6 +1459,21 @@ cudaError_t launch_fill_staged_relu(const uint32_t* stage, const int32_t* stage_
     return cudaGetLastError();
 }
 
+bool fused_fill_ok(int n_tiles) { return n_tiles <= kFusedFillMaxTiles; }
+
+cudaError_t launch_layout_fill_relu(const uint32_t* stage, const int32_t* stage_cnt, int NB, int BN, int stride,
+                                    const TwellView& tw, int sm_count, int32_t* status, cudaStream_t s)
+{
+    if (!fused_fill_ok(tw.n_tiles)) return cudaErrorInvalidValue;
+    // one block per SM, each filling a contiguous share of the rows
+    const int blocks = sm_count > 0 ? sm_count : 1;
+    const int rows_per_block = (tw.M + blocks - 1) / blocks;
+    const int grid = (tw.M + rows_per_block - 1) / rows_per_block;
+    count_launches(1);
+    k_layout_fill_relu<<<grid, 1024, 0, s>>>(stage, stage_cnt, NB, BN, stride, tw, rows_per_block, status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_overflow_rows(const TwellView& tw, int C, int cap_rows, int32_t* ov_pos, int32_t* ov_rows,
                                  int32_t* n_rows, int32_t* status, cudaStream_t s)
 {
@@ -1400,18 +1505,19 @@ cudaError_t launch_fill_staged_gate(const uint2* stage, const int32_t* stage_cnt
 static cudaError_t launch_gather(int src, const GatherArgs& ga, int ntasks, int32_t* status, cudaStream_t s)
 {
     count_launches(1);
-    if (ga.d > 256) {
-        const int64_t tasks = (int64_t)ntasks * ((ga.d + 511) / 512);
+    const int ch = ga.d > 256 ? 2 : 1;
+    const int64_t tasks = (int64_t)ntasks * ((ga.d + 256 * ch - 1) / (256 * ch));
+    const unsigned grid = (unsigned)((tasks + kGatherWarps - 1) / kGatherWarps);
+    if (ch == 2) {
         if (src == SRC_TWELL)
-            k_gather<2, SRC_TWELL><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(ga, status);
+            k_gather<2, SRC_TWELL><<<grid, kGatherWarps * 32, 0, s>>>(ga, status);
         else
-            k_gather<2, SRC_CSC><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(ga, status);
+            k_gather<2, SRC_CSC><<<grid, kGatherWarps * 32, 0, s>>>(ga, status);
     } else {
-        const int64_t tasks = (int64_t)ntasks * ((ga.d + 255) / 256);
         if (src == SRC_TWELL)
-            k_gather<1, SRC_TWELL><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(ga, status);
+            k_gather<1, SRC_TWELL><<<grid, kGatherWarps * 32, 0, s>>>(ga, status);
         else
-            k_gather<1, SRC_CSC><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(ga, status);
+            k_gather<1, SRC_CSC><<<grid, kGatherWarps * 32, 0, s>>>(ga, status);
     }
     return cudaGetLastError();
 }
