@@ -77,12 +77,14 @@ cudaError_t launch_layout_fill_small_relu(const uint32_t* stage, const int32_t* 
 // or an fp32 array indexed by slot.
 cudaError_t launch_spmm_rows(const TwellView& tw, const float* vals_f32, const uint16_t* W, int d,
                              uint16_t* y, int32_t* status, cudaStream_t s);
-// dpre[slot] = dy[r] . W[idx] + l1 on stored slots, 0 on padding. The dot
-// products run over column slices of up to 1024 columns; part holds
-// sddmm_slices(d) * tw.cap floats of per-slice sums (workspace).
+// The SDDMM's dot products dy[r] . W[idx] on the stored slots, over column
+// slices of up to 1024 columns: part holds sddmm_slices(d) * tw.cap floats of
+// per-slice sums (workspace). launch_sddmm_combine_scatter (after the column
+// lists' index kernels) then adds them into dpre[slot] (+ l1 on stored slots,
+// 0 on padding) and scatters every entry's row, h and dpre into the lists.
 int sddmm_slices(int d);
-cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float l1,
-                         float* dpre, float* part, int32_t* status, cudaStream_t s);
+cudaError_t launch_sddmm_slices(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float* part,
+                                int32_t* status, cudaStream_t s);
 // Gated: val[slot] = bf16(relu(g) * (x[r] . W_up[idx])) on stored slots.
 cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16_t* W_up, int d,
                             const float* gval, int32_t* status, cudaStream_t s);
@@ -102,9 +104,10 @@ void csc_plan(int M, int F, int* row_blocks, int* rows_per_block);
 // Column lists of the stored entries: masks, per-(block, column) starts and
 // column pointers (the TwELL indices only) ...
 cudaError_t launch_csc_lists(const TwellView& tw, const CscWork& w, int32_t* status, cudaStream_t s);
-// ... then every entry's row, h and dpre at its place (dpre: [slots], by slot).
-cudaError_t launch_csc_scatter(const TwellView& tw, const CscWork& w, const float* dpre, int32_t* status,
-                               cudaStream_t s);
+// ... then dpre from the SDDMM's slice sums, and every entry's row, h and dpre
+// at its place in the lists.
+cudaError_t launch_sddmm_combine_scatter(const TwellView& tw, int d, const float* part, float l1, float* dpre,
+                                         const CscWork& w, int32_t* status, cudaStream_t s);
 // dW_down[j] = sum h dy[r], dW_up[j] = sum dpre x[r], db[j] = sum dpre over column j.
 cudaError_t launch_wgrad(const TwellView& tw, const CscWork& w, const float* dpre, const uint16_t* x,
                          const uint16_t* dy, int d, float* dW_up, float* dW_down, float* db, int32_t* status,

@@ -575,13 +575,14 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
         timer_end(TWELL_SITE_CSC, s);
     }
     timer_begin(TWELL_SITE_SDDMM, s);
-    if (e == cudaSuccess) e = launch_sddmm(tw, dy, W_down, d, l1_coef, w.dpre, w.part, status, s);
+    if (e == cudaSuccess) e = launch_sddmm_slices(tw, dy, W_down, d, w.part, status, s);
+    // the column lists' positions are needed from here on
+    if (e == cudaSuccess && side) e = cudaStreamWaitEvent(s, side->join, 0);
+    if (e == cudaSuccess) e = launch_sddmm_combine_scatter(tw, d, w.part, l1_coef, w.dpre, w.csc, status, s);
     timer_end(TWELL_SITE_SDDMM, s);
     timer_begin(TWELL_SITE_DX, s);
     if (e == cudaSuccess) e = launch_spmm_rows(tw, w.dpre, W_up, d, dx, status, s);
     timer_end(TWELL_SITE_DX, s);
-    if (e == cudaSuccess && side) e = cudaStreamWaitEvent(s, side->join, 0);
-    if (e == cudaSuccess) e = launch_csc_scatter(tw, w.csc, w.dpre, status, s);
     timer_begin(TWELL_SITE_WGRAD, s);
     if (e == cudaSuccess) e = launch_wgrad(tw, w.csc, w.dpre, x, dy, d, dW_up, dW_down, db, status, s);
     timer_end(TWELL_SITE_WGRAD, s);

@@ -1142,7 +1142,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32) k_gather(GatherArgs ga, con
 // go in batches of 32, two at a time (2 NCH 128-bit loads in flight per
 // lane), each lane forming its columns' share of both dot products;
 // transpose_reduce32 then leaves entry u's slice sum in lane u, written to
-// part[s * cap + slot]. k_sddmm_combine adds the slices in order.
+// part[s * cap + slot]. k_sddmm_combine_scatter adds the slices in order.
 template <int NCH>
 __global__ void __launch_bounds__(kWarps * 32) k_sddmm_slices(TwellView tw, const uint16_t* __restrict__ dy,
                                                               const uint16_t* __restrict__ W, int d, int nslices,
@@ -1196,30 +1196,6 @@ __global__ void __launch_bounds__(kWarps * 32) k_sddmm_slices(TwellView tw, cons
         }
         transpose_reduce32(v, lane);
         if (lane < m) out[k0 + lane] = v[0];
-    }
-}
-
-// dpre[slot] = (part[0][slot] + part[1][slot] + ...) + l1 on the stored slots
-// of row r (slices added in order), 0 on its padding. One warp per row.
-__global__ void __launch_bounds__(kWarps * 32) k_sddmm_combine(TwellView tw, const float* __restrict__ part,
-                                                               int nslices, float l1, float* __restrict__ dpre,
-                                                               const int32_t* status)
-{
-    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
-    int Kt;
-    const int64_t base = row_base(tw, r, &Kt);
-    const int n = tw.nnz[r];
-    for (int k = lane; k < Kt; k += 32) {
-        const int64_t slot = base + k;
-        float v = 0.f;
-        if (k < n) {
-            v = part[slot];
-            for (int sl = 1; sl < nslices; ++sl) v += part[(size_t)sl * (size_t)tw.cap + slot];
-            v += l1;
-        }
-        dpre[slot] = v;
     }
 }
 
@@ -1397,29 +1373,42 @@ __global__ void __launch_bounds__(1024) k_scan_i32(const int32_t* __restrict__ c
     if (tid == 1023) ptr[n] = run;
 }
 
-// Each entry goes to its place in its column's list with its row, its h and
-// its dpre: the weight-gradient kernel then reads them with coalesced loads
-// instead of every one of its column-group warps gathering them by slot.
-__global__ void k_csc_scatter(TwellView tw, const unsigned long long* __restrict__ masks,
-                              const int32_t* __restrict__ start, const int32_t* __restrict__ colptr,
-                              const float* __restrict__ dpre, int32_t* __restrict__ crow,
-                              uint16_t* __restrict__ cval, float* __restrict__ cdpre, const int32_t* status)
+// The SDDMM's last step and the column lists' scatter in one pass, a warp per
+// row: dpre[slot] = (part[0][slot] + part[1][slot] + ...) + l1 on the stored
+// slots of row r (slices added in order), 0 on its padding; and each stored
+// entry goes to its place in its column's list with its row, its h and its
+// dpre, so that the weight-gradient gathers read them with coalesced loads.
+// An entry's place is colptr[j] + start[b][j] + the popcount of the mask
+// bits below its row.
+__global__ void __launch_bounds__(kWarps * 32) k_sddmm_combine_scatter(
+    TwellView tw, const float* __restrict__ part, int nslices, float l1, float* __restrict__ dpre,
+    const unsigned long long* __restrict__ masks, const int32_t* __restrict__ start,
+    const int32_t* __restrict__ colptr, int32_t* __restrict__ crow, uint16_t* __restrict__ cval,
+    float* __restrict__ cdpre, const int32_t* status)
 {
     const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (r >= tw.M || has_error(status)) return;
+    if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
     int Kt;
     const int64_t base = row_base(tw, r, &Kt);
     const int n = tw.nnz[r];
     const int b = r / kCscRows;
     const unsigned long long below = (1ull << (r - b * kCscRows)) - 1ull;
-    for (int k = lane; k < n; k += 32) {
-        const int j = tw.idx[base + k];
-        const size_t bj = (size_t)b * tw.F + j;
-        const int pos = colptr[j] + start[bj] + __popcll(masks[bj] & below);
-        crow[pos] = r;
-        cval[pos] = tw.val[base + k];
-        cdpre[pos] = dpre[base + k];
+    for (int k = lane; k < Kt; k += 32) {
+        const int64_t slot = base + k;
+        float v = 0.f;
+        if (k < n) {
+            v = part[slot];
+            for (int sl = 1; sl < nslices; ++sl) v += part[(size_t)sl * (size_t)tw.cap + slot];
+            v += l1;
+            const int j = tw.idx[slot];
+            const size_t bj = (size_t)b * tw.F + j;
+            const int pos = colptr[j] + start[bj] + __popcll(masks[bj] & below);
+            crow[pos] = r;
+            cval[pos] = tw.val[slot];
+            cdpre[pos] = v;
+        }
+        dpre[slot] = v;
     }
 }
 
@@ -1580,8 +1569,8 @@ static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const
 
 int sddmm_slices(int d) { return (d + 1023) / 1024; }
 
-cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float l1, float* dpre,
-                         float* part, int32_t* status, cudaStream_t s)
+cudaError_t launch_sddmm_slices(const TwellView& tw, const uint16_t* dy, const uint16_t* W, int d, float* part,
+                                int32_t* status, cudaStream_t s)
 {
     // slices of up to four 256-column chunks (1024 columns)
     const int nch_total = (d + 255) / 256;
@@ -1589,14 +1578,13 @@ cudaError_t launch_sddmm(const TwellView& tw, const uint16_t* dy, const uint16_t
     const int nsl = (nch_total + nch - 1) / nch;
     if (nsl > sddmm_slices(d)) return cudaErrorInvalidValue;
     const int64_t tasks = (int64_t)tw.M * nsl;
-    count_launches(2);
+    count_launches(1);
     switch (nch) {
         case 1: k_sddmm_slices<1><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, dy, W, d, nsl, part, status); break;
         case 2: k_sddmm_slices<2><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, dy, W, d, nsl, part, status); break;
         case 3: k_sddmm_slices<3><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, dy, W, d, nsl, part, status); break;
         default: k_sddmm_slices<4><<<grid_for_warps(tasks), kWarps * 32, 0, s>>>(tw, dy, W, d, nsl, part, status); break;
     }
-    k_sddmm_combine<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, part, nsl, l1, dpre, status);
     return cudaGetLastError();
 }
 
@@ -1717,12 +1705,15 @@ cudaError_t launch_csc_lists(const TwellView& tw, const CscWork& w, int32_t* sta
     return cudaGetLastError();
 }
 
-cudaError_t launch_csc_scatter(const TwellView& tw, const CscWork& w, const float* dpre, int32_t* status,
-                               cudaStream_t s)
+cudaError_t launch_sddmm_combine_scatter(const TwellView& tw, int d, const float* part, float l1, float* dpre,
+                                         const CscWork& w, int32_t* status, cudaStream_t s)
 {
+    const int nch_total = (d + 255) / 256;
+    const int nch = nch_total < 4 ? nch_total : 4;
+    const int nsl = (nch_total + nch - 1) / nch;
     count_launches(1);
-    k_csc_scatter<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, w.masks, w.start, w.colptr, dpre, w.crow,
-                                                               w.cval, w.cdpre, status);
+    k_sddmm_combine_scatter<<<grid_for_warps(tw.M), kWarps * 32, 0, s>>>(tw, part, nsl, l1, dpre, w.masks, w.start,
+                                                                           w.colptr, w.crow, w.cval, w.cdpre, status);
     return cudaGetLastError();
 }
 
