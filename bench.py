@@ -524,14 +524,15 @@ def energy_leg(tw, local_rank: int, runs: dict, tokens: int, seconds: float = 2.
 # SHA-256 of the source file it was built from: once that file changes the
 # figure no longer describes the kernel and the site reports traffic null.
 NCU_TRAFFIC = {
-    # training workload, profiles/ncu_fwd_bwd_training_M16384.md; a call site's
-    # figure is the sum over its launches (site 3: the slices and the combine;
-    # site 6: the dW_down and the dW_up gathers)
+    # training workload, from the ncu summary of that step under profiles/; a call site's
+    # figure is the sum over its launches (site 3: the slices and the combine,
+    # which also scatters the column lists; site 6: the dW_down and the dW_up
+    # gathers)
     ("training", 1): ("twell_gemm.cu", "805eb0973a54da0d6f6cb4aa8684ad01ad0b8e508dbcc0da74b9a7c9dd3f241c", 1390.0e6),
-    ("training", 2): ("twell_sparse.cu", "13c3ed8fa111f102332285262d735a587adaa3452034bc8262e8e67d52cd3eee", 304.1e6),
-    ("training", 3): ("twell_sparse.cu", "13c3ed8fa111f102332285262d735a587adaa3452034bc8262e8e67d52cd3eee", 411.7e6),
-    ("training", 4): ("twell_sparse.cu", "13c3ed8fa111f102332285262d735a587adaa3452034bc8262e8e67d52cd3eee", 345.4e6),
-    ("training", 6): ("twell_sparse.cu", "13c3ed8fa111f102332285262d735a587adaa3452034bc8262e8e67d52cd3eee", 918.0e6),
+    ("training", 2): ("twell_sparse.cu", "7b06a0417762934d0ac078c6ad160f1456b26ca40776db3502daf47176565b27", 303.1e6),
+    ("training", 3): ("twell_sparse.cu", "7b06a0417762934d0ac078c6ad160f1456b26ca40776db3502daf47176565b27", 508.2e6),
+    ("training", 4): ("twell_sparse.cu", "7b06a0417762934d0ac078c6ad160f1456b26ca40776db3502daf47176565b27", 345.3e6),
+    ("training", 6): ("twell_sparse.cu", "7b06a0417762934d0ac078c6ad160f1456b26ca40776db3502daf47176565b27", 917.1e6),
 }
 
 
@@ -562,8 +563,8 @@ def site_work(site: int, inp, slots: int, nnz: int):
         return 2.0 * M * d * F, M * d * 2 + F * d * 2 + nnz * 4 + F * 4
     if site == 2:  # y = TwELL W_down
         return 2.0 * nnz * d, F * d * 2 + slots * 6 + M * d * 2
-    if site == 3:  # dpre on the stored slots
-        return 2.0 * nnz * d, M * d * 2 + F * d * 2 + slots * 4 + slots * 4
+    if site == 3:  # dpre on the stored slots, then each entry's row, h, dpre into the column lists
+        return 2.0 * nnz * d, M * d * 2 + F * d * 2 + slots * (4 + 2) + slots * 4 + nnz * 10
     if site == 4:  # dx = dpre W_up
         return 2.0 * nnz * d, F * d * 2 + slots * 8 + M * d * 2
     if site == 5:  # column lists: masks, counts, pointers (TwELL indices only)
