@@ -155,6 +155,8 @@ def test_fwd_integer_inputs_bit_exact():
     (200, 256, 1024, 128, -1.0, 1),    # several tiles, ragged last row tile
     (130, 136, 264, 7, -0.5, 2),       # ragged K (d % 64 != 0), F % 256 != 0, odd T
     (712, 200, 800, 64, -1.2, 3),      # several 256 x 256 pair tiles each way, ragged in M, N and K
+    (1100, 64, 2304, 16, -1.5, 4),     # more rows than the small-batch fill: one-launch layout and fill
+    (2100, 64, 256, 1, -1.0, 5),       # more tiles than that launch holds: separate layout and fill
 ])
 def test_fwd_relu_matches_oracle(M, d, F, T, bias, seed):
     inp = syn.ffn_inputs(M, d, F, T, bias, seed=seed)
@@ -309,6 +311,39 @@ def test_bwd_is_deterministic():
     b = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, 1e-3)
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u, v)
+
+
+def test_bwd_ragged_slices_groups_and_row_blocks():
+    """d = 1288: two SDDMM slices of 1024 columns, the second ending 8 columns
+    into its second 256-column chunk, and a last 512-column gather group of 264
+    columns; M = 300: four 64-row column-list blocks and a ragged fifth;
+    F = 776; tiles of 64 rows with a ragged last tile. Every output element
+    against the oracle."""
+    M, d, F, T, l1 = 300, 1288, 776, 64, 1e-3
+    h = syn.sparse_hidden(M, F, 0.03, seed=31)
+    inp = syn.ffn_inputs(M, d, F, T, -2.0, seed=31, with_dy=True)
+    ref_tw = oracle.twell_pack(h, T)
+    dx, dWu, dWd, db = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, l1)
+    X, Wu, Wd, H, DY = (bf16_f64(a) for a in (inp.x, inp.W_up, inp.W_down, h, inp.dy))
+    _, dx_ref = oracle.ffn_bwd_rows(X, Wu, Wd, H, DY, l1)
+    gu, gd, gb = oracle.ffn_bwd_cols(X, Wu, Wd, H, DY, l1)
+    assert_close_rms(dx, dx_ref, what="dx", bf16_out=True)
+    assert_close_rms(dWu, gu, what="dW_up")
+    assert_close_rms(dWd, gd, what="dW_down")
+    assert_close_rms(db, gb, what="db")
+
+
+def test_bwd_of_an_empty_hidden_matrix_is_zero():
+    """No active unit anywhere (K = 0 in every tile, no slots): dx, dW_up,
+    dW_down and db are exactly zero, as the oracle's definition gives."""
+    M, d, F, T = 130, 256, 512, 32
+    h = syn.sparse_hidden(M, F, 0.0, seed=32)
+    inp = syn.ffn_inputs(M, d, F, T, -2.0, seed=32, with_dy=True)
+    ref_tw = oracle.twell_pack(h, T)
+    assert ref_tw.slots == 0
+    dx, dWu, dWd, db = _bwd(inp.x, inp.W_up, inp.W_down, ref_tw, inp.dy, 1e-2)
+    for a in (dx, dWu, dWd, db):
+        assert np.all(a == 0)
 
 
 # ------------------------------------------------------ dense baseline ------
