@@ -289,6 +289,9 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            // the gate GEMM streams W_gate once: its lines go first, so that the
+            // W_up / W_down rows the epilogue prefetches for the next kernel stay
+            const uint64_t pol_a = l2_policy_evict_first();
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int mb = tile % num_m, nb = tile / num_m;
                 // gate GEMM: each tile starts at its own k so that the CTAs do not
@@ -305,7 +308,10 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int sub = 0; sub < KSUB; ++sub) {
                         uint8_t* ss = sa + sub * L::SUB_BYTES;
-                        tma_load_2d(ss, &tmA, (kb + sub) * BK, mb * BM, &full[stage]);
+                        if constexpr (MODE == GEMM_GATE_SWAP)
+                            tma_load_2d_hint(ss, &tmA, (kb + sub) * BK, mb * BM, &full[stage], pol_a);
+                        else
+                            tma_load_2d(ss, &tmA, (kb + sub) * BK, mb * BM, &full[stage]);
                         tma_load_2d(ss + L::A_BYTES, &tmB, (kb + sub) * BK, nb * BN, &full[stage]);
                     }
                     ++issued;
@@ -428,8 +434,8 @@ __global__ void __launch_bounds__(192, 1)
                         const int jj = mb * BM + 32 * q + __ffs(units) - 1;
                         units &= units - 1;
                         for (int off = lane * 128; off < a.pf_row_bytes; off += 32 * 128) {
-                            prefetch_l2(reinterpret_cast<const char*>(a.pf0) + (size_t)jj * a.pf_row_bytes + off);
-                            prefetch_l2(reinterpret_cast<const char*>(a.pf1) + (size_t)jj * a.pf_row_bytes + off);
+                            prefetch_l2_keep(reinterpret_cast<const char*>(a.pf0) + (size_t)jj * a.pf_row_bytes + off);
+                            prefetch_l2_keep(reinterpret_cast<const char*>(a.pf1) + (size_t)jj * a.pf_row_bytes + off);
                         }
                     }
                 }

@@ -705,37 +705,71 @@ __global__ void __launch_bounds__(kTailWarps * 32, 1)
     if (has_error(status)) return;
 
     // ---------------------------------------------------------------- A --
-    for (int i = tid; i < nseg; i += blockDim.x) sm.pre[i] = stage_cnt[i];
+    // eight independent loads in flight per thread: at 64 tokens the staged
+    // counts are 14 per thread, and one at a time they cost a round trip each
+    for (int i0 = tid; i0 < nseg; i0 += 8 * kTailWarps * 32) {
+        int c[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * kTailWarps * 32;
+            c[q] = i < nseg ? __ldcg(stage_cnt + i) : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * kTailWarps * 32;
+            if (i < nseg) sm.pre[i] = c[q];
+        }
+    }
     __syncthreads();
+    // one warp per token, four consecutive counts per lane and round
     for (int t = warp; t < M; t += kTailWarps) {
+        int* pt = sm.pre + t * NB;
         int carry = 0;
-        for (int nb0 = 0; nb0 < NB; nb0 += 32) {
-            const int nb = nb0 + lane;
-            const int c = nb < NB ? sm.pre[t * NB + nb] : 0;
-            const int incl = warp_incl_scan(c, lane);
-            if (nb < NB) sm.pre[t * NB + nb] = carry + incl - c;
+        for (int nb0 = 0; nb0 < NB; nb0 += 128) {
+            const int b0 = nb0 + lane * 4;
+            int c[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) c[u] = b0 + u < NB ? pt[b0 + u] : 0;
+            const int sum = c[0] + c[1] + c[2] + c[3];
+            const int incl = warp_incl_scan(sum, lane);
+            int run = carry + incl - sum;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (b0 + u < NB) pt[b0 + u] = run;
+                run += c[u];
+            }
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) s_nnz[t] = carry;
     }
     __syncthreads();
+    // tile widths (one warp per tile), the tokens' entry prefix (warp 0 over
+    // M <= 64 tokens, two per lane), then the tile offsets in order
+    for (int tt = warp; tt < tw.n_tiles; tt += kTailWarps) {
+        const int r0 = tt * tw.T, rows = min(tw.T, M - r0);
+        int mx = 0;
+        for (int i = lane; i < rows; i += 32) mx = max(mx, s_nnz[r0 + i]);
+        mx = warp_max_i(mx);
+        if (lane == 0) s_K[tt] = mx;
+    }
+    if (warp == 0) {
+        const int a0 = lane < M ? s_nnz[lane] : 0;
+        const int a1 = lane + 32 < M ? s_nnz[lane + 32] : 0;
+        const int i0 = warp_incl_scan(a0, lane);
+        const int tot0 = __shfl_sync(0xffffffffu, i0, 31);
+        const int i1 = warp_incl_scan(a1, lane) + tot0;
+        if (lane < M) s_tok[lane] = i0 - a0;
+        if (lane + 32 < M) s_tok[lane + 32] = i1 - a1;
+        if (lane == 31) s_tok[M] = i1;
+    }
+    __syncthreads();
     if (tid == 0) {
         long long off = 0;
         for (int tt = 0; tt < tw.n_tiles; ++tt) {
-            const int r0 = tt * tw.T, rows = min(tw.T, M - r0);
-            int mx = 0;
-            for (int i = 0; i < rows; ++i) mx = max(mx, s_nnz[r0 + i]);
-            s_K[tt] = mx;
             s_off[tt] = off;
-            off += (long long)rows * mx;
+            off += (long long)min(tw.T, M - tt * tw.T) * s_K[tt];
         }
         s_off[tw.n_tiles] = off;
-        int e = 0;
-        for (int t = 0; t < M; ++t) {
-            s_tok[t] = e;
-            e += s_nnz[t];
-        }
-        s_tok[M] = e;
     }
     __syncthreads();
     const bool over = s_off[tw.n_tiles] > tw.cap;
