@@ -627,6 +627,29 @@ def stage_roofline(name, ms, inp, slots, nnz, peaks):
             "algorithmic": f"{by / 1e6:.1f} MB compulsory"}
 
 
+def call_roofline(sites, ms_call: float, inp, slots: int, nnz: int, peaks, ceil: dict):
+    """Roofline fraction of one library call: the sum over its kernels of
+    max(compulsory bytes / HBM peak, FLOPs / pipe peak) over the measured call
+    time (bf16 tensor peak for the GEMM, the measured FP32 FMA rate for the
+    CUDA-core kernels). "attainable" adds each gather's L2-to-SM bytes at the
+    measured gather ceiling as a third bound."""
+    hbm, fma, bf16 = peaks["hbm"] * 1e9, ceil["fma_tflops"] * 1e12, peaks["bf16"] * 1e12
+    t_roof = t_att = 0.0
+    parts = {}
+    for site in sites:
+        flops, byts = site_work(site, inp, slots, nnz)
+        t = max(byts / hbm, flops / (bf16 if site == 1 else fma))
+        g = GATHER_ROWS.get(site, 0) * nnz * inp.d * 2 / (ceil["gather_tbs"] * 1e12)
+        t_roof += t
+        t_att += max(t, g)
+        parts[SITES[site]] = {"roofline_us": t * 1e6, "attainable_us": max(t, g) * 1e6}
+    s = ms_call / 1000.0
+    return {"frac": t_roof / s, "roofline_ms": t_roof * 1e3, "attainable_frac": t_att / s,
+            "attainable_ms": t_att * 1e3, "ms": ms_call, "kernels": parts,
+            "rule": "sum over kernels of max(bytes / HBM, FLOPs / pipe peak) / call time; attainable adds "
+                    "gathered bytes / measured L2-to-SM gather ceiling"}
+
+
 class L2Flush:
     """Evicts L2 between timed steps: writes a buffer larger than L2 (129 MB),
     then reads another one, so that the lines left behind are clean. (Writing
@@ -1203,7 +1226,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clocks,
-        "fwd": {"value": world * inp.M / (ms_fwd / 1000.0), "unit": UNIT, "ms": ms_fwd},
+        "fwd": {"value": world * inp.M / (ms_fwd / 1000.0), "unit": UNIT, "ms": ms_fwd,
+                "call_roofline": call_roofline((1, 2), ms_fwd, inp, slots, nnz, peaks, ceil)},
+        "step_roofline": call_roofline((1, 2, 3, 4, 5, 6), ms_step, inp, slots, nnz, peaks, ceil),
         "stages": stages,
         "kernels": kernels,
         "ceilings": {"fma": fma, "gather_TBs": gath, "hbm_GBs": peaks["hbm"], "bf16_TFLOPs": peaks["bf16"]},
