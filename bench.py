@@ -528,11 +528,11 @@ NCU_TRAFFIC = {
     # figure is the sum over its launches (site 3: the slices and the combine,
     # which also scatters the column lists; site 6: the dW_down and the dW_up
     # gathers)
-    ("training", 1): ("twell_gemm.cu", "805eb0973a54da0d6f6cb4aa8684ad01ad0b8e508dbcc0da74b9a7c9dd3f241c", 1390.0e6),
-    ("training", 2): ("twell_sparse.cu", "7b06a0417762934d0ac078c6ad160f1456b26ca40776db3502daf47176565b27", 303.1e6),
-    ("training", 3): ("twell_sparse.cu", "7b06a0417762934d0ac078c6ad160f1456b26ca40776db3502daf47176565b27", 508.2e6),
-    ("training", 4): ("twell_sparse.cu", "7b06a0417762934d0ac078c6ad160f1456b26ca40776db3502daf47176565b27", 345.3e6),
-    ("training", 6): ("twell_sparse.cu", "7b06a0417762934d0ac078c6ad160f1456b26ca40776db3502daf47176565b27", 917.1e6),
+    ("training", 1): ("twell_gemm.cu", "71f0a49a5c1005032c85e734d4c012c661369eef59b56b204fc992bb6fc25ded", 1387.6e6),
+    ("training", 2): ("twell_sparse.cu", "848859bbb7332392464ba8967cce6013c426e7a31f0d3c2b1829b7e5ebabfe41", 302.8e6),
+    ("training", 3): ("twell_sparse.cu", "848859bbb7332392464ba8967cce6013c426e7a31f0d3c2b1829b7e5ebabfe41", 507.6e6),
+    ("training", 4): ("twell_sparse.cu", "848859bbb7332392464ba8967cce6013c426e7a31f0d3c2b1829b7e5ebabfe41", 345.5e6),
+    ("training", 6): ("twell_sparse.cu", "848859bbb7332392464ba8967cce6013c426e7a31f0d3c2b1829b7e5ebabfe41", 917.0e6),
 }
 
 
@@ -666,12 +666,12 @@ class L2Flush:
         self.sink = torch.amax(self.r)
 
 
-def decode_leg(tw, peaks, flush, stream, reps: int = 30):
+def decode_leg(tw, peaks, flush, stream, reps: int = 30, batches=(1, 8, 64)):
     """Gated decode forward (M = 1, 8, 64 tokens, d_model 4096, d_ff 14336, ~99.5 % sparse):
     time of one twell_ffn_fwd call with L2 flushed before it, and its HBM roofline
     (algorithmic bytes: W_gate once, the union of active W_up and W_down rows once, x, y)."""
     out = {}
-    for name in ("decode1", "decode8", "decode64"):
+    for name in (f"decode{m}" for m in batches):
         inp = syn.config_inputs(name)
         M, d, F, T = inp.M, inp.d, inp.F, inp.T
         x, Wu, Wg, Wd = dev16(inp.x), dev16(inp.W_up), dev16(inp.W_gate), dev16(inp.W_down)
@@ -1201,7 +1201,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         torch.cuda.empty_cache()
         memory = training_memory_leg(tw, inp, L1)
     inference = inference_leg(tw, flush, stream, peaks)[0] if leg_on(args, "inference") else None
-    decode = decode_leg(tw, peaks, flush, stream) if leg_on(args, "decode") else None
+    decode = (decode_leg(tw, peaks, flush, stream, batches=tuple(int(m) for m in args.decode_batches.split(",")))
+              if leg_on(args, "decode") else None)
     hybrid = hybrid_leg(tw, flush, stream) if leg_on(args, "hybrid") else None
 
     cpu = None
@@ -1255,6 +1256,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e, dense and CPU legs (profiling runs)")
+    ap.add_argument("--decode-batches", default="1,8,64",
+                    help="token counts of the decode leg's gated workloads (of 1, 8, 64)")
     ap.add_argument("--legs", default="all",
                     help="comma list of the extra legs to run: e2e, dense, crossover, inference, energy, memory, down, "
                          "decode, hybrid "
