@@ -6,8 +6,8 @@ One step = the whole hot path over one batch of the training workload
 hidden activations zero, TwELL tiles of 128 rows, dy ~ N(0,1), L1 coefficient
 1e-4 on h):
 
-    twell_up_pack    tcgen05 up-projection, TwELL built in its epilogue (a1-a3)
-    twell_spmm_down  y = TwELL x W_down                                     (a4)
+    twell_ffn_fwd    tcgen05 up-projection, TwELL built in its epilogue (a1-a3),
+                     then y = TwELL x W_down (a4)
     twell_ffn_bwd    dpre, dx, column lists, dW_up, dW_down, db             (a6-a9)
 
 Inputs are resident in HBM when the timed region starts; L2 is flushed (a
@@ -279,12 +279,6 @@ class Layer:
         self.dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
         self.dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
         self.db = torch.empty(F, dtype=torch.float32, device="cuda")
-
-    def up(self):
-        self.tw.twell_up_pack(self.x, self.Wu, None, self.b, self.inp.T, self.buf, self.ws_f, self.st)
-
-    def down(self):
-        self.tw.twell_spmm_down(self.buf, self.Wd, self.y, self.st)
 
     def fwd(self):
         self.tw.twell_ffn_fwd(self.x, self.Wu, None, self.b, self.Wd, self.inp.T, self.buf, self.y, self.ws_f,
@@ -612,13 +606,13 @@ def kernel_roofline(site: int, us: float, inp, slots: int, nnz: int, peaks, ceil
 def stage_roofline(name, ms, inp, slots, nnz, peaks):
     M, d, F = inp.M, inp.d, inp.F
     s = ms / 1000.0
-    if name == "up_pack":
+    if name == "ffn_fwd":
         flops = 2.0 * M * d * F
         a = flops / s / 1e12
         return {"bound": "tensor", "achieved": a, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                "frac": a / peaks["bf16"], "algorithmic": f"{flops / 1e9:.1f} GFLOP (2 M d_model d_ff)"}
-    if name == "spmm_down":
-        by = F * d * 2 + slots * 6 + M * d * 2
+                "frac": a / peaks["bf16"],
+                "algorithmic": f"{flops / 1e9:.1f} GFLOP (2 M d_model d_ff, the up GEMM; the gather's "
+                               f"{2.0 * nnz * d / 1e9:.1f} GFLOP not counted)"}
     else:
         # compulsory: x, dy, W_up, W_down, TwELL read once; dx, dW_up, dW_down, db written once
         by = 2 * M * d * 2 + 2 * F * d * 2 + slots * 6 + M * d * 2 + 2 * F * d * 4 + F * 4
@@ -953,7 +947,7 @@ def crossover_leg(tw, L: "Layer", flush, stream, dense_step_ms, reps: int = 5):
     try:
         for name, bias in CROSSOVER_BIASES.items():
             L.b = torch.full_like(b0, bias)
-            ms = timed_ms(lambda: (L.up(), L.down(), L.bwd()), flush, stream, L.st, tw, n=reps)
+            ms = timed_ms(lambda: (L.fwd(), L.bwd()), flush, stream, L.st, tw, n=reps)
             nnz = int(L.buf.nnz.sum().item())
             out[name] = {"bias": bias, "density": nnz / (L.inp.M * L.inp.F), "step_ms": ms,
                          "tokens_per_s": L.inp.M / (ms / 1000.0)}
@@ -1068,16 +1062,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     def step(evs):
         evs[0].record(stream)
-        L.up()
+        L.fwd()
         evs[1].record(stream)
-        L.down()
-        evs[2].record(stream)
         L.bwd()
-        evs[3].record(stream)
+        evs[2].record(stream)
 
     for i in range(args.warmup):
         flush.fill_(i & 0xff)
-        step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
     L.check("warm-up")
     slots = L.buf.slots()
     nnz = int(L.buf.nnz.sum().item())
@@ -1092,14 +1084,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             b2.record(stream)
             tw.twell_set_kernel_timer(site, a, b2)
             flush.fill_(i & 0xff)
-            step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+            step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
             evs.append((a, b2))
         tw.twell_set_kernel_timer(0)
         torch.cuda.synchronize()
         site_us[site] = statistics.mean(a.elapsed_time(b2) for a, b2 in evs[1:]) * 1000.0
     dom_site = dominant_site(site_us)
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b2 in kev:
         a.record(stream)
@@ -1126,13 +1118,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     clocks = sampler.stop()
     L.check("timed steps")
 
-    up = [e[0].elapsed_time(e[1]) for e in events]
-    down = [e[1].elapsed_time(e[2]) for e in events]
-    bwd = [e[2].elapsed_time(e[3]) for e in events]
-    ms = {"up_pack": statistics.mean(up), "spmm_down": statistics.mean(down), "ffn_bwd": statistics.mean(bwd)}
+    fwd = [e[0].elapsed_time(e[1]) for e in events]
+    bwd = [e[1].elapsed_time(e[2]) for e in events]
+    ms = {"ffn_fwd": statistics.mean(fwd), "ffn_bwd": statistics.mean(bwd)}
     ms_step = max_over_ranks(sum(ms.values()), world)
     value = whole_job_rate(inp.M, world, ms_step)
-    ms_fwd = ms["up_pack"] + ms["spmm_down"]
+    ms_fwd = ms["ffn_fwd"]
 
     # ---- measured ceilings of the CUDA-core kernels (probes.cu, same run)
     sms = tw.twell_device_sm_count()
@@ -1182,7 +1173,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     energy = None
     if leg_on(args, "energy"):
-        runs = {"twell_step": lambda: (L.up(), L.down(), L.bwd())}
+        runs = {"twell_step": lambda: (L.fwd(), L.bwd())}
         if D is not None:
             runs["dense_step"] = lambda: (D.fwd(), D.bwd())
         energy = energy_leg(tw, local_rank, runs, inp.M)

@@ -595,6 +595,62 @@ def test_fwd_staging_overflow_is_reported():
     assert tw.twell_check(st) == 4  # TWELL_ERR_CAPACITY
 
 
+def _up_pack_then_down(inp):
+    M, d, F, T = inp.M, inp.d, inp.F, inp.T
+    buf = tw.TwellBuffers(M, F, T, M * F)
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    ws = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_FWD, M, d, F, T, M * F), dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    tw.twell_up_pack(dev_bf16(inp.x), dev_bf16(inp.W_up), None, dev_f32(inp.b), T, buf, ws, st)
+    tw.twell_spmm_down(buf, dev_bf16(inp.W_down), y, st)
+    return buf, y, st
+
+
+@pytest.mark.parametrize("M,d,F,T,bias,seed", [
+    (520, 264, 776, 64, -1.5, 11),     # ragged rows, columns and blocks
+    (260, 136, 2048, 32, 0.5, 12),     # ~70 % active: blocks of ~180 staged entries
+    (1100, 64, 2304, 16, -2.33, 13),   # the one-launch layout and fill
+])
+def test_fwd_matches_up_pack_then_spmm_down(M, d, F, T, bias, seed):
+    """The one-call forward and the two calls it is made of (up-projection
+    with TwELL packing, then the TwELL down-projection) give the same TwELL
+    and y, bit for bit."""
+    inp = syn.ffn_inputs(M, d, F, T, bias, seed=seed)
+    buf1, y1, st1 = _fwd(inp)
+    _status_ok(st1)
+    buf2, y2, st2 = _up_pack_then_down(inp)
+    _status_ok(st2)
+    assert_twell_identical(twell_to_host(buf1), twell_to_host(buf2))
+    np.testing.assert_array_equal(host_bf16_bits(y1), host_bf16_bits(y2))
+    ref = oracle.ffn_fwd_rows(inp.x, inp.W_up, None, inp.b, inp.W_down, M, d, F)
+    assert_close_rms(bf16_f64(host_bf16_bits(y1)), ref["y"], what="y", bf16_out=True)
+
+
+def test_fwd_replayed_from_a_cuda_graph_matches_eager():
+    """The forward recorded in a CUDA graph (how a serving loop would issue
+    it): replays give the eager TwELL and y bit for bit."""
+    M, d, F, T = 300, 264, 520, 32
+    inp = syn.ffn_inputs(M, d, F, T, -1.5, seed=14)
+    buf_e, y_e, st_e = _fwd(inp)  # eager, also creates the side stream
+    _status_ok(st_e)
+    ref_tw, ref_y = twell_to_host(buf_e), host_bf16_bits(y_e)
+    x, Wu, Wd, b = dev_bf16(inp.x), dev_bf16(inp.W_up), dev_bf16(inp.W_down), dev_f32(inp.b)
+    buf = tw.TwellBuffers(M, F, T, M * F)
+    y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+    ws = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_FWD, M, d, F, T, M * F), dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tw.twell_ffn_fwd(x, Wu, None, b, Wd, T, buf, y, ws, st)
+    for _ in range(2):
+        y.zero_(), buf.idx.zero_(), buf.val.zero_()
+        g.replay()
+        _status_ok(st)
+        assert_twell_identical(twell_to_host(buf), ref_tw)
+        np.testing.assert_array_equal(host_bf16_bits(y), ref_y)
+
+
 def test_bwd_replayed_from_a_cuda_graph_matches_eager():
     """The backward forks its index-only column-list kernels onto a side stream
     and joins them back by events; captured in a CUDA graph and replayed it must
