@@ -73,6 +73,24 @@ __device__ __forceinline__ void transpose_reduce32(float (&v)[32], int lane)
     }
 }
 
+// The same over 16 values: lane u (and lane u + 16) ends with the sum over all
+// 32 lanes of v[u & 15] in v[0] (15 shuffles within each half-warp, then one
+// across the halves).
+__device__ __forceinline__ void transpose_reduce16(float (&v)[16], int lane)
+{
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
