@@ -634,16 +634,15 @@ struct GatherArgs {
 // 16384 rows) and that slice stays in L2, whatever the size of W. Lane l holds
 // columns 256 CH g + 256 c + 8 l .. +7 of chunk c; entries come 4 at a time
 // (4 CH 128-bit loads in flight per lane).
-// Blocks of 4 warps: measured against 8 at the training size, the gathers
-// finish 1-3 % sooner (a finer grid balances the last wave better). Seven
-// blocks per SM (72 registers, a few bytes spilled on the tail path) instead
-// of the six that 80 registers allow: 28 warps keep more rows' loads in
-// flight, 3-4 % faster at the training size; eight (64 registers) spill in
-// the main loop and are slower.
-constexpr int kGatherWarps = 4;
+// Small blocks balance the last wave: 4 warps finish 1-3 % sooner than 8 at
+// the training size, 2 warps another ~1 % (weight gradients). 28 warps per SM
+// (72 registers, a few bytes spilled on the tail path) instead of the 24 that
+// 80 registers allow keep more rows' loads in flight: 3-4 % faster; 32 warps
+// (64 registers) spill in the main loop and are slower.
+constexpr int kGatherWarps = 2;
 
 template <int CH, int SRC>
-__global__ void __launch_bounds__(kGatherWarps * 32, 7) k_gather(GatherArgs ga, const int32_t* status)
+__global__ void __launch_bounds__(kGatherWarps * 32, 14) k_gather(GatherArgs ga, const int32_t* status)
 {
     constexpr int GW = 256 * CH;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
