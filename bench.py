@@ -522,11 +522,11 @@ NCU_TRAFFIC = {
     # figure is the sum over its launches (site 3: the slices and the combine,
     # which also scatters the column lists; site 6: the dW_down and the dW_up
     # gathers)
-    ("training", 1): ("twell_gemm.cu", "71f0a49a5c1005032c85e734d4c012c661369eef59b56b204fc992bb6fc25ded", 1387.6e6),
-    ("training", 2): ("twell_sparse.cu", "6f5a510409c6456b2e1019a4b28df8df6f8e094b12ee14c16c3c86f1f35b3c01", 310.4e6),
-    ("training", 3): ("twell_sparse.cu", "6f5a510409c6456b2e1019a4b28df8df6f8e094b12ee14c16c3c86f1f35b3c01", 509.0e6),
-    ("training", 4): ("twell_sparse.cu", "6f5a510409c6456b2e1019a4b28df8df6f8e094b12ee14c16c3c86f1f35b3c01", 355.6e6),
-    ("training", 6): ("twell_sparse.cu", "6f5a510409c6456b2e1019a4b28df8df6f8e094b12ee14c16c3c86f1f35b3c01", 939.2e6),
+    ("training", 1): ("twell_gemm.cu", "71f0a49a5c1005032c85e734d4c012c661369eef59b56b204fc992bb6fc25ded", 1293.7e6),
+    ("training", 2): ("twell_sparse.cu", "c2c369d579a769655bf4301fce74cf2bb12b414ba89fddf43d9ea1f927d69124", 310.6e6),
+    ("training", 3): ("twell_sparse.cu", "c2c369d579a769655bf4301fce74cf2bb12b414ba89fddf43d9ea1f927d69124", 511.5e6),
+    ("training", 4): ("twell_sparse.cu", "c2c369d579a769655bf4301fce74cf2bb12b414ba89fddf43d9ea1f927d69124", 355.1e6),
+    ("training", 6): ("twell_sparse.cu", "c2c369d579a769655bf4301fce74cf2bb12b414ba89fddf43d9ea1f927d69124", 938.9e6),
 }
 
 
