@@ -548,7 +548,7 @@ twell_status twell_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const uint16
         return TWELL_ERR_INVALID_ARG;
     twell_status st = check_buf(h, M, F, h->T);
     if (st != TWELL_OK) return st;
-    if (h->cap_slots >= (int64_t)INT32_MAX || d > 4096) return TWELL_ERR_UNSUPPORTED;
+    if (h->cap_slots >= (int64_t)INT32_MAX) return TWELL_ERR_UNSUPPORTED;
     const size_t need = carve_bwd(nullptr, M, d, F, h->cap_slots, nullptr);
     if (!ws || ws_bytes < need) return TWELL_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TWELL_ERR_INVALID_ARG;

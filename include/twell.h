@@ -272,8 +272,8 @@ twell_status twell_hybrid_ffn_bwd(const uint16_t* x, const uint16_t* W_up, const
  *   h: the forward's TwELL; ws: at least twell_workspace_bytes(TWELL_OP_FFN_BWD,
  *   M, d, F, T, h->cap_slots) bytes, 256-byte aligned (it grows with d: the
  *   dot products of dpre are summed over column slices of 1024, one fp32 per
- *   stored slot and slice). Limits of this build: d <= 4096,
- *   h->cap_slots < 2^31 (else TWELL_ERR_UNSUPPORTED).
+ *   stored slot and slice). Limit of this build: h->cap_slots < 2^31 (else
+ *   TWELL_ERR_UNSUPPORTED).
  * The reduction order of every sum is fixed (no floating-point atomics).
  * The column lists' index-only kernels run on the library's side stream while
  * the SDDMM runs on `stream`; the call's work is complete when `stream`'s is.

@@ -268,6 +268,7 @@ def _bwd(x, W_up, W_down, ref_tw, dy, l1):
     (64, 128, 512, 16, -2.33, 1e-4, 0),
     (150, 264, 520, 32, -1.5, 0.0, 1),
     (90, 64, 1024, 128, -1.0, 5e-2, 2),
+    (70, 8200, 264, 16, -1.5, 1e-3, 3),   # d_model past 8192: nine SDDMM slices, the last one ragged
 ])
 def test_bwd_matches_oracle(M, d, F, T, bias, l1, seed):
     inp = syn.ffn_inputs(M, d, F, T, bias, seed=seed, with_dy=True)
