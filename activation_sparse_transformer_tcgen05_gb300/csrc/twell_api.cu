@@ -179,7 +179,6 @@ twell_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TWELL_OK : T
 bool dims_ok(int M, int d, int F) { return M > 0 && d > 0 && F > 0 && d % 8 == 0 && F % 8 == 0; }
 
 // Limits of this build's kernels.
-constexpr int kMaxD = 4096;  // the gated up products keep 16 chunks of 256 columns per warp in registers
 constexpr int kUnionMaxF = 65536;  // the union kernel keeps a group's bucket starts in shared memory
 
 }  // namespace
@@ -328,7 +327,6 @@ twell_status up_pack_impl(const uint16_t* x, const uint16_t* W_up, const uint16_
     twell_status st = check_buf(h_out, M, F, T);
     if (st != TWELL_OK) return st;
     const bool gated = W_gate != nullptr;
-    if (gated && d > kMaxD) return TWELL_ERR_UNSUPPORTED;
     // ReLU: the epilogue staging holds as many entries per (row, 256-column
     // block) as the workspace allows (the "predicted N_nz" capacity); gated:
     // full blocks

@@ -828,16 +828,14 @@ __global__ void __launch_bounds__(kSddmmWarps * 32, 7)
     }
 }
 
-// Row dot products on the stored entries: for entry (r, k) with column j,
-// s = A[r] . W[j]. MODE 0 (backward SDDMM): out[slot] = s + l1 on stored slots
-// and 0 on padding. MODE 1 (gated up): val[slot] = bf16(g * s), g = gval[slot].
-// WPR warps share a row, entry k going to warp k % WPR; a row's A slice stays
-// in registers (NCH chunks of 256 columns, 8 per lane).
-template <int NCH, int MODE>
+// Gated up products, row-parallel: for stored entry (r, k) with column j,
+// s = A[r] . W[j] and val[slot] = bf16(relu(g) * s), g = gval[slot]. WPR warps
+// share a row, entry k going to warp k % WPR; a row's A slice stays in
+// registers (NCH chunks of 256 columns, 8 per lane).
+template <int NCH>
 __global__ void __launch_bounds__(kWarps * 32) k_row_dots(TwellView tw, const uint16_t* __restrict__ A,
-                                                          const uint16_t* __restrict__ W, int d, int wpr, float l1,
-                                                          float* __restrict__ out, const float* __restrict__ gval,
-                                                          const int32_t* status)
+                                                          const uint16_t* __restrict__ W, int d, int wpr,
+                                                          const float* __restrict__ gval, const int32_t* status)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * (kWarps / wpr) + warp / wpr;
@@ -891,15 +889,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_row_dots(TwellView tw, const ui
         }
         if (lane < m) {
             const int64_t s = base + kl;
-            if (MODE == 0) {
-                out[s] = res + l1;
-            } else {
-                tw.val[s] = f32_to_bf16_bits(fmaxf(gval[s], 0.f) * res);
-            }
+            tw.val[s] = f32_to_bf16_bits(fmaxf(gval[s], 0.f) * res);
         }
-    }
-    if (MODE == 0 && sub == 0) {
-        for (int k = n + lane; k < Kt; k += 32) out[base + k] = 0.f;
     }
 }
 
@@ -1159,9 +1150,8 @@ cudaError_t launch_spmm_rows(const TwellView& tw, const float* vals_f32, const u
     return cudaGetLastError();
 }
 
-template <int MODE>
-static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const uint16_t* W, int d, float l1,
-                                   float* out, const float* gval, int32_t* status, cudaStream_t s)
+static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const uint16_t* W, int d,
+                                   const float* gval, int32_t* status, cudaStream_t s)
 {
     const int nch = (d + 255) / 256;
     const int wpr = tw.M >= 256 ? 1 : kWarps;
@@ -1169,7 +1159,7 @@ static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const
     count_launches(1);
 #define TWELL_ROWDOT_CASE(N)                                                                      \
     case N:                                                                                       \
-        k_row_dots<N, MODE><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, l1, out, gval, status); \
+        k_row_dots<N><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, gval, status); \
         break;
     switch (nch) {
         TWELL_ROWDOT_CASE(1)
@@ -1184,9 +1174,9 @@ static cudaError_t launch_row_dots(const TwellView& tw, const uint16_t* A, const
         TWELL_ROWDOT_CASE(16)
         default:
             if (nch <= 12) {
-                k_row_dots<12, MODE><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, l1, out, gval, status);
+                k_row_dots<12><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, gval, status);
             } else if (nch <= 16) {
-                k_row_dots<16, MODE><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, l1, out, gval, status);
+                k_row_dots<16><<<grid, kWarps * 32, 0, s>>>(tw, A, W, d, wpr, gval, status);
             } else {
                 return cudaErrorInvalidValue;
             }
@@ -1219,13 +1209,14 @@ cudaError_t launch_sddmm_slices(const TwellView& tw, const uint16_t* dy, const u
 cudaError_t launch_gated_up(const TwellView& tw, const uint16_t* x, const uint16_t* W_up, int d, const float* gval,
                             int32_t* status, cudaStream_t s)
 {
-    if (tw.M <= 256) {
-        // few rows: spread the slots over the whole GPU, a warp per slot
+    if (tw.M <= 256 || (d + 255) / 256 > 16) {
+        // few rows: spread the slots over the whole GPU, a warp per slot (also
+        // for d_model beyond the 16 chunks the row-parallel kernel holds)
         count_launches(1);
         k_gated_up_slots<<<2 * 152, kWarps * 32, 0, s>>>(tw, x, W_up, d, gval, status);
         return cudaGetLastError();
     }
-    return launch_row_dots<1>(tw, x, W_up, d, 0.f, nullptr, gval, status, s);
+    return launch_row_dots(tw, x, W_up, d, gval, status, s);
 }
 
 bool small_fill_ok(int M, int NB) { return M <= 1024 && (long long)M * NB <= kSmallFillMax; }

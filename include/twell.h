@@ -179,7 +179,7 @@ twell_status twell_spmm_down_tc(const twell_buf* h, const uint16_t* W_down, int 
  *   h_out: TwELL of h (M, F, T as given), its val holding h.
  *   ws: device workspace of at least twell_workspace_bytes(TWELL_OP_FFN_FWD or
  *   TWELL_OP_GATED_FWD, M, d, F, T, h_out->cap_slots) bytes, 256-byte aligned;
- *   contents need no init. Gated mode limit of this build: d <= 4096.
+ *   contents need no init.
  * Capacity overflow of h_out: nnz/K/off are written, slots and y are not, and
  * *status = TWELL_ERR_CAPACITY.
  */

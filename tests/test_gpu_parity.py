@@ -197,6 +197,8 @@ def test_fwd_gated_decode(name):
     (100, 256, 1024, 32, 4),     # two token chunks of the gate GEMM; layout+fill and slot-parallel up products
     (300, 264, 1032, 64, 5),     # more than 256 rows: row-parallel up products; ragged d, F and tiles
     (40, 136, 520, 40, 6),       # a decode batch with ragged d and F (one cooperative tail)
+    (300, 4360, 520, 64, 7),     # d_model past 4096 with more than 256 rows: slot-parallel up products
+    (1, 4360, 1040, 1, 8),       # ... and as a one-token decode (the tail loops over the columns)
 ])
 def test_fwd_gated_beyond_decode(M, d, F, T, seed):
     _check_gated(syn.ffn_inputs(M, d, F, T, -1.5, seed=seed, gated=True))
