@@ -522,11 +522,11 @@ NCU_TRAFFIC = {
     # figure is the sum over its launches (site 3: the slices and the combine,
     # which also scatters the column lists; site 6: the dW_down and the dW_up
     # gathers)
-    ("training", 1): ("twell_gemm.cu", "71f0a49a5c1005032c85e734d4c012c661369eef59b56b204fc992bb6fc25ded", 1293.7e6),
-    ("training", 2): ("twell_sparse.cu", "c2c369d579a769655bf4301fce74cf2bb12b414ba89fddf43d9ea1f927d69124", 310.6e6),
-    ("training", 3): ("twell_sparse.cu", "c2c369d579a769655bf4301fce74cf2bb12b414ba89fddf43d9ea1f927d69124", 511.5e6),
-    ("training", 4): ("twell_sparse.cu", "c2c369d579a769655bf4301fce74cf2bb12b414ba89fddf43d9ea1f927d69124", 355.1e6),
-    ("training", 6): ("twell_sparse.cu", "c2c369d579a769655bf4301fce74cf2bb12b414ba89fddf43d9ea1f927d69124", 938.9e6),
+    ("training", 1): ("twell_gemm.cu", "71f0a49a5c1005032c85e734d4c012c661369eef59b56b204fc992bb6fc25ded", 1293.1e6),
+    ("training", 2): ("twell_sparse.cu", "73630e9b399f34d99b8cf1393b7a2df84d4b7028d514acf5b4a6bc5631f81613", 310.4e6),
+    ("training", 3): ("twell_sparse.cu", "73630e9b399f34d99b8cf1393b7a2df84d4b7028d514acf5b4a6bc5631f81613", 511.2e6),
+    ("training", 4): ("twell_sparse.cu", "73630e9b399f34d99b8cf1393b7a2df84d4b7028d514acf5b4a6bc5631f81613", 355.9e6),
+    ("training", 6): ("twell_sparse.cu", "73630e9b399f34d99b8cf1393b7a2df84d4b7028d514acf5b4a6bc5631f81613", 939.0e6),
 }
 
 
