@@ -130,9 +130,59 @@ __global__ void k_fill_dense(const uint16_t* __restrict__ h, int ldh, TwellView 
 
 // Slots of row r (a warp) from the up-projection epilogue's staging: the row's
 // column blocks are concatenated in block order (each block's entries are
-// already ascending), then padded.
-// With ov_pos (hybrid format), rows routed to the dense overflow block
-// (ov_pos[r] >= 0) are left empty here: padding only.
+// already ascending), then padded. Blocks go 64 at a time (two per lane), and
+// the first four entries of both of a lane's blocks are loaded before any is
+// stored, so that at ~1 % density (2.6 entries per block) a row costs two
+// dependent round trips instead of one per entry.
+__device__ __forceinline__ void fill_row_staged(const uint32_t* __restrict__ stage,
+                                                const int32_t* __restrict__ stage_cnt, int NB, int nb_end, int BN,
+                                                int stride, const TwellView& tw, int r, int64_t base, int Kt, int lane)
+{
+    int pos = 0;
+    for (int nb0 = 0; nb0 < nb_end; nb0 += 64) {
+        int c[2], incl[2];
+        const uint32_t* src[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int nb = nb0 + 32 * h + lane;
+            c[h] = nb < nb_end ? stage_cnt[(size_t)r * NB + nb] : 0;
+            src[h] = stage + ((size_t)r * NB + nb) * stride;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) incl[h] = warp_incl_scan(c[h], lane);
+        const int tot0 = __shfl_sync(0xffffffffu, incl[0], 31);
+        uint32_t w[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[h][q] = q < c[h] ? src[h][q] : 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int nb = nb0 + 32 * h + lane;
+            const int64_t p = base + pos + (h ? tot0 : 0) + (incl[h] - c[h]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (q < c[h]) {
+                    tw.idx[p + q] = nb * BN + (int)(w[h][q] & 0xffffu);
+                    tw.val[p + q] = (uint16_t)(w[h][q] >> 16);
+                }
+            }
+            for (int e = 4; e < c[h]; ++e) {  // denser blocks
+                const uint32_t v = src[h][e];
+                tw.idx[p + e] = nb * BN + (int)(v & 0xffffu);
+                tw.val[p + e] = (uint16_t)(v >> 16);
+            }
+        }
+        pos += tot0 + __shfl_sync(0xffffffffu, incl[1], 31);
+    }
+    for (int k = pos + lane; k < Kt; k += 32) {
+        tw.idx[base + k] = -1;
+        tw.val[base + k] = 0;
+    }
+}
+
+// A warp per row. With ov_pos (hybrid format), rows routed to the dense
+// overflow block (ov_pos[r] >= 0) are left empty here: padding only.
 __global__ void k_fill_staged_relu(const uint32_t* __restrict__ stage, const int32_t* __restrict__ stage_cnt, int NB,
                                    int BN, int stride, TwellView tw, const int32_t* __restrict__ ov_pos,
                                    const int32_t* status)
@@ -142,25 +192,8 @@ __global__ void k_fill_staged_relu(const uint32_t* __restrict__ stage, const int
     if (r >= tw.M || has_error(status) || over_capacity(tw)) return;
     int Kt;
     const int64_t base = row_base(tw, r, &Kt);
-    int pos = 0;
     const int nb_end = (ov_pos && ov_pos[r] >= 0) ? 0 : NB;
-    for (int nb0 = 0; nb0 < nb_end; nb0 += 32) {
-        const int nb = nb0 + lane;
-        const int c = nb < NB ? stage_cnt[(size_t)r * NB + nb] : 0;
-        const int incl = warp_incl_scan(c, lane);
-        const int64_t p = base + pos + (incl - c);
-        const uint32_t* src = stage + ((size_t)r * NB + nb) * stride;
-        for (int e = 0; e < c; ++e) {
-            const uint32_t w = src[e];
-            tw.idx[p + e] = nb * BN + (int)(w & 0xffffu);
-            tw.val[p + e] = (uint16_t)(w >> 16);
-        }
-        pos += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    for (int k = pos + lane; k < Kt; k += 32) {
-        tw.idx[base + k] = -1;
-        tw.val[base + k] = 0;
-    }
+    fill_row_staged(stage, stage_cnt, NB, nb_end, BN, stride, tw, r, base, Kt, lane);
 }
 
 // Layout and fill of the ReLU TwELL in one launch (n_tiles <= kFusedFillMaxTiles):
@@ -228,24 +261,7 @@ __global__ void __launch_bounds__(1024) k_layout_fill_relu(const uint32_t* __res
     for (int r = r_begin + warp; r < r_end; r += 32) {
         const int t = r / tw.T, Kt = s_K[t];
         const int64_t base = s_off[t] + (int64_t)(r - t * tw.T) * Kt;
-        int pos = 0;
-        for (int nb0 = 0; nb0 < NB; nb0 += 32) {
-            const int nb = nb0 + lane;
-            const int c = nb < NB ? stage_cnt[(size_t)r * NB + nb] : 0;
-            const int ic = warp_incl_scan(c, lane);
-            const int64_t p = base + pos + (ic - c);
-            const uint32_t* src = stage + ((size_t)r * NB + nb) * stride;
-            for (int e = 0; e < c; ++e) {
-                const uint32_t w = src[e];
-                tw.idx[p + e] = nb * BN + (int)(w & 0xffffu);
-                tw.val[p + e] = (uint16_t)(w >> 16);
-            }
-            pos += __shfl_sync(0xffffffffu, ic, 31);
-        }
-        for (int k = pos + lane; k < Kt; k += 32) {
-            tw.idx[base + k] = -1;
-            tw.val[base + k] = 0;
-        }
+        fill_row_staged(stage, stage_cnt, NB, NB, BN, stride, tw, r, base, Kt, lane);
     }
 }
 
