@@ -523,10 +523,10 @@ NCU_TRAFFIC = {
     # which also scatters the column lists; site 6: the dW_down and the dW_up
     # gathers)
     ("training", 1): ("twell_gemm.cu", "71f0a49a5c1005032c85e734d4c012c661369eef59b56b204fc992bb6fc25ded", 1293.1e6),
-    ("training", 2): ("twell_sparse.cu", "73630e9b399f34d99b8cf1393b7a2df84d4b7028d514acf5b4a6bc5631f81613", 310.4e6),
-    ("training", 3): ("twell_sparse.cu", "73630e9b399f34d99b8cf1393b7a2df84d4b7028d514acf5b4a6bc5631f81613", 511.2e6),
-    ("training", 4): ("twell_sparse.cu", "73630e9b399f34d99b8cf1393b7a2df84d4b7028d514acf5b4a6bc5631f81613", 355.9e6),
-    ("training", 6): ("twell_sparse.cu", "73630e9b399f34d99b8cf1393b7a2df84d4b7028d514acf5b4a6bc5631f81613", 939.0e6),
+    ("training", 2): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 310.6e6),
+    ("training", 3): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 511.2e6),
+    ("training", 4): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 354.5e6),
+    ("training", 6): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 938.9e6),
 }
 
 
