@@ -515,10 +515,12 @@ constexpr int HALF = 128;     // rows of A and of B held by one CTA
 
 // Tile order of the CTA-pair kernel: groups of kRasterN consecutive column
 // tiles; inside a group the column tile varies fastest. The ~76 pairs at work
-// at any time then cover about 10 row tiles x 8 column tiles, whose A rows and
-// B rows (~40 MB at K = 4096) stay in L2, so A is read from DRAM once per
-// group instead of once per column tile.
-constexpr int kRasterN = 8;
+// at any time then cover about 5 row tiles x 16 column tiles, whose A rows and
+// B rows (~42 MB at K = 4096) stay in L2, so A is read from DRAM once per
+// group instead of once per column tile. At 16384 x 16384 x 4096: 16 column
+// tiles per group 1.6-2 % faster than 8, 32 slower (its group's rows no
+// longer stay in L2), 4 slower still.
+constexpr int kRasterN = 16;
 
 __device__ __forceinline__ void pair_tile_coords(int tile, int num_m, int num_n, int* mb, int* nb)
 {

@@ -522,7 +522,7 @@ NCU_TRAFFIC = {
     # figure is the sum over its launches (site 3: the slices and the combine,
     # which also scatters the column lists; site 6: the dW_down and the dW_up
     # gathers)
-    ("training", 1): ("twell_gemm.cu", "71f0a49a5c1005032c85e734d4c012c661369eef59b56b204fc992bb6fc25ded", 1293.1e6),
+    ("training", 1): ("twell_gemm.cu", "11f75b785884244dfff061adb2d7ded88b99df5d227cc3baf38622fe112db28b", 813.3e6),
     ("training", 2): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 310.6e6),
     ("training", 3): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 511.2e6),
     ("training", 4): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 354.5e6),
