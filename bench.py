@@ -522,25 +522,41 @@ NCU_TRAFFIC = {
     # figure is the sum over its launches (site 3: the slices and the combine,
     # which also scatters the column lists; site 6: the dW_down and the dW_up
     # gathers)
-    ("training", 1): ("twell_gemm.cu", "11f75b785884244dfff061adb2d7ded88b99df5d227cc3baf38622fe112db28b", 813.3e6),
-    ("training", 2): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 310.6e6),
-    ("training", 3): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 511.2e6),
-    ("training", 4): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 354.5e6),
-    ("training", 6): ("twell_sparse.cu", "b4adef9b191b9ed2aa35442a8c24c7f135cc1cdc4a72509ec8ba216138982370", 938.9e6),
+    ("training", 1): ("twell_gemm.cu", "787b72d9dc15eecd18efb32473080d26db82d17f855a5870c857c92fb2f102f9", 813.3e6),
+    ("training", 2): ("twell_sparse.cu", "42b071ee146ebaf6a8b4676ead682fa924bb798e16a0309fe3a524371086b17d", 311.1e6),
+    ("training", 3): ("twell_sparse.cu", "42b071ee146ebaf6a8b4676ead682fa924bb798e16a0309fe3a524371086b17d", 511.2e6),
+    ("training", 4): ("twell_sparse.cu", "42b071ee146ebaf6a8b4676ead682fa924bb798e16a0309fe3a524371086b17d", 356.3e6),
+    ("training", 6): ("twell_sparse.cu", "42b071ee146ebaf6a8b4676ead682fa924bb798e16a0309fe3a524371086b17d", 935.1e6),
 }
 
 
+# The sources a kernel's code comes from: its translation unit and the
+# library headers it includes, hashed together in this order.
+KERNEL_SOURCES = {
+    "twell_gemm.cu": ("common.cuh", "launch.h", "twell_gemm.cu"),
+    "twell_sparse.cu": ("common.cuh", "launch.h", "sparse_common.cuh", "twell_sparse.cu"),
+}
+
+
+def source_digest(unit: str):
+    """SHA-256 over the bytes of a translation unit's sources (None if one is missing)."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[unit]:
+        try:
+            with open(os.path.join(ROOT, "activation_sparse_transformer_tcgen05_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    return h.hexdigest()
+
+
 def ncu_traffic(site: int, workload: str):
+    """The committed ncu DRAM traffic of a call site, or None once its kernels'
+    sources differ from the ones the counters were taken on."""
     ent = NCU_TRAFFIC.get((workload, site))
     if ent is None:
         return None
-    path = os.path.join(ROOT, "activation_sparse_transformer_tcgen05_gb300", "csrc", ent[0])
-    try:
-        with open(path, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-    except OSError:
-        return None
-    return ent[2] if digest == ent[1] else None
+    return ent[2] if source_digest(ent[0]) == ent[1] else None
 
 
 # Rows of d bf16 each sparse kernel pulls through L2 per stored entry:

@@ -65,6 +65,16 @@ __global__ void __launch_bounds__(256) k_fma(int iters, float seed, float* sink)
 // --------------------------------------------------------------- gathers --
 
 constexpr int kWarps = 8;
+constexpr int kColsWarps = 2;  // the down-projection's block: 2 warps, 14 blocks per SM
+
+// 16 bytes from read-only global memory, in the same form as the library's
+// gathers (a plain inline-PTX load).
+__device__ __forceinline__ uint4 ldg16(const uint16_t* p)
+{
+    uint4 v;
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
 
 // One warp per (row r, 256-column group g): for k < nnz the lane reads the 16
 // bytes at W[idx[r, k], 256 g + 8 lane], IN_FLIGHT 128-bit loads at a time.
@@ -109,17 +119,18 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_ldg(const uint16_t* __re
     if (lane == 0) sink[task] = __uint_as_float(acc & 0x007fffffu);
 }
 
-// The down-projection's own order: warp task (column group g of 512 columns,
-// row r), task = g * rows + r, so the grid walks W one 512-column slice at a
-// time; the lane reads 16 bytes in each of its two 256-column chunks, four
-// entries (eight 128-bit loads) in flight.
-__global__ void __launch_bounds__(kWarps * 32) k_gather_cols(const uint16_t* __restrict__ W, int F, int d,
-                                                             const int32_t* __restrict__ idx, int rows, int nnz,
-                                                             float* __restrict__ sink)
+// The down-projection's own order and launch shape: warp task (column group g
+// of 512 columns, row r), task = g * rows + r, so the grid walks W one
+// 512-column slice at a time; the lane reads 16 bytes in each of its two
+// 256-column chunks, four entries (eight 128-bit loads) in flight; 2-warp
+// blocks, 14 per SM.
+__global__ void __launch_bounds__(kColsWarps * 32, 14) k_gather_cols(const uint16_t* __restrict__ W, int F, int d,
+                                                                     const int32_t* __restrict__ idx, int rows,
+                                                                     int nnz, float* __restrict__ sink)
 {
     const int lane = threadIdx.x & 31;
     const int G = (d + 511) >> 9;
-    const long long task = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const long long task = (long long)blockIdx.x * kColsWarps + (threadIdx.x >> 5);
     if (task >= (long long)rows * G) return;
     const int g = (int)(task / rows), r = (int)(task % rows);
     const int c0 = g * 512 + lane * 8, c1 = c0 + 256;
@@ -136,10 +147,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_cols(const uint16_t* __r
             for (int q = 0; q < 4; ++q) {
                 const int j = __shfl_sync(0xffffffffu, jl, u + q < m ? u + q : u);
                 const bool live = u + q < m;
-                v[q][0] = (live && ok0) ? __ldg(reinterpret_cast<const uint4*>(W + (size_t)j * d + c0))
-                                        : make_uint4(0, 0, 0, 0);
-                v[q][1] = (live && ok1) ? __ldg(reinterpret_cast<const uint4*>(W + (size_t)j * d + c1))
-                                        : make_uint4(0, 0, 0, 0);
+                v[q][0] = (live && ok0) ? ldg16(W + (size_t)j * d + c0) : make_uint4(0, 0, 0, 0);
+                v[q][1] = (live && ok1) ? ldg16(W + (size_t)j * d + c1) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -298,9 +307,9 @@ int probe_gather(int mode, const uint16_t* W, int F, int d, const int32_t* idx, 
             k_gather_ldg<8><<<(unsigned)blocks, kWarps * 32, 0, s>>>(W, F, d, idx, rows, nnz, sink);
     } else if (mode == 4) {
         const long long t4 = (long long)rows * ((d + 511) / 512);
-        const long long blocks = (t4 + kWarps - 1) / kWarps;
+        const long long blocks = (t4 + kColsWarps - 1) / kColsWarps;
         if (blocks > 0x7fffffffLL) return 1;
-        k_gather_cols<<<(unsigned)blocks, kWarps * 32, 0, s>>>(W, F, d, idx, rows, nnz, sink);
+        k_gather_cols<<<(unsigned)blocks, kColsWarps * 32, 0, s>>>(W, F, d, idx, rows, nnz, sink);
     } else if (mode == 2 || mode == 3) {
         if (d % 256 != 0) return 1;
         const long long blocks = (tasks + kBulkWarps - 1) / kBulkWarps;
