@@ -654,6 +654,54 @@ def test_fwd_replayed_from_a_cuda_graph_matches_eager():
         np.testing.assert_array_equal(host_bf16_bits(y), ref_y)
 
 
+def test_fwd_and_bwd_from_two_threads_on_two_streams():
+    """Two host threads, each on its own stream with its own buffers, run the
+    forward and the backward (whose column-list kernels go to a side stream
+    of the calling thread) at the same time: each gets what it gets alone."""
+    import threading
+    cases = [syn.ffn_inputs(300, 264, 520, 32, -1.5, seed=s, with_dy=True) for s in (21, 22)]
+
+    def run(inp, stream):
+        M, d, F, T = inp.M, inp.d, inp.F, inp.T
+        with torch.cuda.stream(stream):
+            buf = tw.TwellBuffers(M, F, T, M * F)
+            y = torch.empty(M, d, dtype=torch.int16, device="cuda")
+            wsf = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_FWD, M, d, F, T, M * F), dtype=torch.uint8,
+                              device="cuda")
+            wsb = torch.empty(tw.twell_workspace_bytes(tw.OP_FFN_BWD, M, d, F, T, M * F), dtype=torch.uint8,
+                              device="cuda")
+            dx = torch.empty(M, d, dtype=torch.int16, device="cuda")
+            dWu = torch.empty(F, d, dtype=torch.float32, device="cuda")
+            dWd = torch.empty(F, d, dtype=torch.float32, device="cuda")
+            db = torch.empty(F, dtype=torch.float32, device="cuda")
+            st = status_tensor()
+            x, Wu, Wd, dy = dev_bf16(inp.x), dev_bf16(inp.W_up), dev_bf16(inp.W_down), dev_bf16(inp.dy)
+            b = dev_f32(inp.b)
+            for _ in range(3):
+                tw.twell_ffn_fwd(x, Wu, None, b, Wd, T, buf, y, wsf, st)
+                tw.twell_ffn_bwd(x, Wu, Wd, buf, dy, 1e-3, dx, dWu, dWd, db, wsb, st)
+            stream.synchronize()
+            return (tw.twell_check(st), host_bf16_bits(y), host_bf16_bits(dx), dWu.cpu().numpy(), dWd.cpu().numpy(),
+                    db.cpu().numpy())
+
+    alone = [run(c, torch.cuda.Stream()) for c in cases]
+    out = [None, None]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+
+    def worker(i):
+        out[i] = run(cases[i], streams[i])
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for got, ref in zip(out, alone):
+        assert got[0] == 0 and ref[0] == 0
+        for u, v in zip(got[1:], ref[1:]):
+            np.testing.assert_array_equal(u, v)
+
+
 def test_bwd_replayed_from_a_cuda_graph_matches_eager():
     """The backward forks its index-only column-list kernels onto a side stream
     and joins them back by events; captured in a CUDA graph and replayed it must
